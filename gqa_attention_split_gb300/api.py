@@ -1,0 +1,254 @@
+"""ctypes binding for libgqa_attn.so — argument marshalling only.
+
+The functions named ``gqa_attn_*`` mirror the C ABI in ``include/gqa_attn.h``
+one to one (raw device pointers as ints, sizes, a ``cudaStream_t`` as an int).
+``decode`` and ``prefill`` are conveniences over them for torch tensors: they
+check dtype/shape/device, allocate outputs, pass ``data_ptr()`` and the current
+stream, and raise ``GqaError`` on a non-zero return code. Every step of the
+computation runs in the library's CUDA kernels; nothing here computes.
+
+The library must be built first (``python -m gqa_attention_split_gb300.build``
+or ``__graft_entry__.build()``); loading fails loudly otherwise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgqa_attn.so")
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = -1
+GQA_ERR_UNSUPPORTED = -2
+GQA_ERR_MISALIGNED = -3
+GQA_ERR_CUDA = -4
+GQA_ERR_DEVICE_TIMEOUT = -5
+GQA_ERR_WORKSPACE = -6
+GQA_ERR_DEVICE_BAD_INPUT = -7
+
+# name -> (restype, argtypes); every symbol include/gqa_attn.h declares.
+_P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGNATURES = {
+    "gqa_attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _S,
+                                _P]),
+    "gqa_attn_decode_workspace_size": (_S, [_I, _I, _I, _I]),
+    "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "gqa_attn_prefill_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "gqa_attn_pick_num_splits": (_I, [_I, _I, _I, _I]),
+    "gqa_attn_split_bounds": (_I, [_I, _I, _I, _P, _P]),
+    "gqa_attn_tile_class": (_I, [_I, _I, _I, _I]),
+    "gqa_attn_prefill_tile_counts": (_I, [_I, _I, _I, _I, _P, _P, _P]),
+    "gqa_attn_prefill_block_m": (_I, []),
+    "gqa_attn_prefill_block_n": (_I, []),
+    "gqa_attn_check": (_I, [_P]),
+    "gqa_attn_strerror": (ctypes.c_char_p, [_I]),
+    "gqa_attn_version": (_I, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GqaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libgqa_attn.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m gqa_attention_split_gb300.build` (CUDA 13, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def symbols():
+    return list(_SIGNATURES)
+
+
+# ---- one-to-one C ABI mirrors --------------------------------------------
+
+
+def gqa_attn_decode(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, num_splits,
+                    stream):
+    return lib().gqa_attn_decode(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale,
+                                 num_splits, stream)
+
+
+def gqa_attn_decode_ws(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, num_splits,
+                       workspace, workspace_bytes, stream):
+    return lib().gqa_attn_decode_ws(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale,
+                                    num_splits, workspace, workspace_bytes, stream)
+
+
+def gqa_attn_decode_workspace_size(B, H_q, d, num_splits):
+    return lib().gqa_attn_decode_workspace_size(B, H_q, d, num_splits)
+
+
+def gqa_attn_prefill(q, k, v, o, lse, B, T_q, S_kv, q_offset, causal, scale, stream):
+    return lib().gqa_attn_prefill(q, k, v, o, lse, B, T_q, S_kv, q_offset, causal, scale,
+                                  stream)
+
+
+def gqa_attn_prefill_ex(q, k, v, o, lse, B, H_q, H_kv, d, T_q, S_kv, q_offset, causal, scale,
+                        stream):
+    return lib().gqa_attn_prefill_ex(q, k, v, o, lse, B, H_q, H_kv, d, T_q, S_kv, q_offset,
+                                     causal, scale, stream)
+
+
+def gqa_attn_pick_num_splits(B, H_kv, S_max, num_sms):
+    return lib().gqa_attn_pick_num_splits(B, H_kv, S_max, num_sms)
+
+
+def gqa_attn_split_bounds(S_max, num_splits, seqlen):
+    """Returns (rc, [(start, end), ...])."""
+    starts = (ctypes.c_int32 * max(num_splits, 1))()
+    ends = (ctypes.c_int32 * max(num_splits, 1))()
+    rc = lib().gqa_attn_split_bounds(S_max, num_splits, seqlen, starts, ends)
+    return rc, [(starts[i], ends[i]) for i in range(max(num_splits, 0))] if rc == 0 else []
+
+
+def gqa_attn_tile_class(qs, qe, ks, ke):
+    return lib().gqa_attn_tile_class(qs, qe, ks, ke)
+
+
+def gqa_attn_prefill_tile_counts(T_q, S_kv, q_offset, causal):
+    """Returns (rc, n_past, n_partial, n_future)."""
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    rc = lib().gqa_attn_prefill_tile_counts(T_q, S_kv, q_offset, causal, ctypes.byref(a),
+                                            ctypes.byref(b), ctypes.byref(c))
+    return rc, a.value, b.value, c.value
+
+
+def gqa_attn_prefill_block_m():
+    return lib().gqa_attn_prefill_block_m()
+
+
+def gqa_attn_prefill_block_n():
+    return lib().gqa_attn_prefill_block_n()
+
+
+def gqa_attn_check(stream=None):
+    return lib().gqa_attn_check(stream)
+
+
+def strerror(code: int) -> str:
+    return lib().gqa_attn_strerror(code).decode()
+
+
+def gqa_attn_version():
+    return lib().gqa_attn_version()
+
+
+# ---- torch conveniences -----------------------------------------------------
+
+
+def _stream_ptr(stream=None):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_cuda_bf16(name, t, ndim):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor, got {tuple(t.shape)}")
+
+
+def decode(q, k, v, seqlens=None, *, num_splits: int = 0, scale: float | None = None,
+           out=None, lse=None, stream=None, workspace=None):
+    """Split-KV decode. q [B,H_q,d], k/v [B,H_kv,S_max,d] bf16 CUDA; seqlens int32 [B] or None.
+
+    Returns (o [B,H_q,d] bf16, lse [B,H_q] fp32). With ``workspace`` (a uint8
+    CUDA tensor) the call goes through gqa_attn_decode_ws.
+    """
+    import torch
+
+    _check_cuda_bf16("q", q, 3)
+    _check_cuda_bf16("k", k, 4)
+    _check_cuda_bf16("v", v, 4)
+    B, H_q, d = q.shape
+    H_kv, S_max = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H_kv, S_max, d] matching q")
+    if seqlens is not None and (seqlens.dtype != torch.int32 or not seqlens.is_cuda
+                                or seqlens.numel() != B):
+        raise TypeError("seqlens must be an int32 CUDA tensor of B elements")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = _stream_ptr(stream)
+    if workspace is None:
+        rc = gqa_attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seqlens),
+                             B, H_q, H_kv, d, S_max, sc, num_splits, st)
+    else:
+        rc = gqa_attn_decode_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                _ptr(seqlens), B, H_q, H_kv, d, S_max, sc, num_splits,
+                                _ptr(workspace), workspace.numel(), st)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_decode")
+    return out, lse
+
+
+def prefill(q, k, v, *, q_offset: int = 0, causal: bool = True, scale: float | None = None,
+            out=None, lse=None, stream=None):
+    """Causal (or full) prefill. q [B,H_q,T_q,d], k/v [B,H_kv,S_kv,d] bf16 CUDA.
+
+    Returns (o [B,H_q,T_q,d] bf16, lse [B,H_q,T_q] fp32).
+    """
+    import torch
+
+    _check_cuda_bf16("q", q, 4)
+    _check_cuda_bf16("k", k, 4)
+    _check_cuda_bf16("v", v, 4)
+    B, H_q, T_q, d = q.shape
+    H_kv, S_kv = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H_kv, S_kv, d] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = gqa_attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv, d,
+                             T_q, S_kv, q_offset, 1 if causal else 0, sc, _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_prefill")
+    return out, lse
+
+
+def check(stream=None):
+    """Synchronises the stream and raises if the device status word is set."""
+    rc = gqa_attn_check(_stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_check")

@@ -1,0 +1,78 @@
+// Integer planning for the decode split-KV sweep and the causal prefill tile
+// schedule. Host only; the kernels recompute the same quantities with the
+// device-side mirrors in plan.cuh, and tests compare both against independent
+// derivations.
+//
+// Page: "ADR-0060: AHBM GQA Fused Attention kernel (Llama3-70B)".
+//   §2.2 valid-length arithmetic  -> split bounds (contiguous chunks here)
+//   §5.4 prefill tile classes     -> gqa_attn_tile_class
+//   §9 tuning (split/tile sizes)  -> gqa_attn_pick_num_splits
+
+#include <algorithm>
+#include <cstdint>
+
+#include "gqa_attn.h"
+#include "plan.cuh"
+
+namespace {
+
+constexpr int kMinKeysPerSplit = 256;   // below this a split is mostly ramp-up
+constexpr int kMaxKeysPerSplit = 1024;  // long rows spread over many blocks
+constexpr int kMaxSplits = 8192;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms) {
+    if (B <= 0 || H_kv <= 0 || S_max <= 0 || num_sms <= 0) return GQA_ERR_INVALID_ARG;
+    const int64_t pairs = int64_t(B) * H_kv;
+    int64_t ns = ceil_div(num_sms, pairs);                     // fill every SM at low batch
+    ns = std::max<int64_t>(ns, ceil_div(S_max, kMaxKeysPerSplit));
+    ns = std::min<int64_t>(ns, std::max(1, S_max / kMinKeysPerSplit));
+    ns = std::max<int64_t>(1, std::min<int64_t>(ns, kMaxSplits));
+    return int(ns);
+}
+
+extern "C" int gqa_attn_split_bounds(int S_max, int num_splits, int seqlen, int32_t* starts,
+                                     int32_t* ends) {
+    if (S_max <= 0 || num_splits <= 0 || seqlen < 0 || seqlen > S_max || !starts || !ends)
+        return GQA_ERR_INVALID_ARG;
+    const int L = gqa::split_len(S_max, num_splits);
+    for (int s = 0; s < num_splits; ++s) {
+        gqa::SplitRange r = gqa::split_range(L, s, seqlen);
+        starts[s] = r.start;
+        ends[s] = r.end;
+    }
+    return GQA_OK;
+}
+
+extern "C" int gqa_attn_tile_class(int qs, int qe, int ks, int ke) {
+    return gqa::tile_class(qs, qe, ks, ke);
+}
+
+extern "C" int gqa_attn_prefill_block_m(void) { return gqa::kPrefillBlockM; }
+extern "C" int gqa_attn_prefill_block_n(void) { return gqa::kPrefillBlockN; }
+
+extern "C" int gqa_attn_prefill_tile_counts(int T_q, int S_kv, int q_offset, int causal,
+                                            int64_t* n_past, int64_t* n_partial,
+                                            int64_t* n_future) {
+    if (T_q < 0 || S_kv < 0 || q_offset < 0 || !n_past || !n_partial || !n_future)
+        return GQA_ERR_INVALID_ARG;
+    int64_t c[3] = {0, 0, 0};
+    const int nm = int(ceil_div(T_q, gqa::kPrefillBlockM));
+    const int nn = int(ceil_div(S_kv, gqa::kPrefillBlockN));
+    for (int i = 0; i < nm; ++i) {
+        const int qs = q_offset + i * gqa::kPrefillBlockM;
+        const int qe = q_offset + std::min((i + 1) * gqa::kPrefillBlockM, T_q);
+        for (int j = 0; j < nn; ++j) {
+            const int ks = j * gqa::kPrefillBlockN;
+            const int ke = std::min((j + 1) * gqa::kPrefillBlockN, S_kv);
+            c[causal ? gqa::tile_class(qs, qe, ks, ke) : gqa::kTileAllPast]++;
+        }
+    }
+    *n_past = c[gqa::kTileAllPast];
+    *n_partial = c[gqa::kTilePartial];
+    *n_future = c[gqa::kTileAllFuture];
+    return GQA_OK;
+}

@@ -1,0 +1,52 @@
+// Integer plan shared by the host library and the kernels (host + device).
+// Page: "ADR-0060: AHBM GQA Fused Attention kernel (Llama3-70B)", §2.2
+// (valid-length arithmetic) and §5.4 (query block vs KV tile classes).
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define GQA_HD __host__ __device__ __forceinline__
+#else
+#define GQA_HD inline
+#endif
+
+namespace gqa {
+
+constexpr int kPrefillBlockM = 128;  // query rows per prefill work item
+constexpr int kPrefillBlockN = 128;  // keys per prefill KV tile
+
+constexpr int kTileAllPast = 0;
+constexpr int kTilePartial = 1;
+constexpr int kTileAllFuture = 2;
+
+struct SplitRange {
+    int start;
+    int end;
+};
+
+// Keys per decode split: L = ceil(S_max / num_splits).
+GQA_HD int split_len(int S_max, int num_splits) {
+    return int((int64_t(S_max) + num_splits - 1) / num_splits);
+}
+
+// Split s covers [s*L, (s+1)*L) on the S_max grid, clipped to [0, seqlen).
+GQA_HD SplitRange split_range(int L, int s, int seqlen) {
+    int64_t a = int64_t(s) * L, b = a + L;
+    SplitRange r;
+    r.start = int(a < seqlen ? a : seqlen);
+    r.end = int(b < seqlen ? b : seqlen);
+    return r;
+}
+
+// Number of non-empty splits of a row: ceil(seqlen / L).
+GQA_HD int active_splits(int L, int seqlen) { return seqlen <= 0 ? 0 : (seqlen + L - 1) / L; }
+
+// §5.4: ke <= qs -> all past; ks >= qe -> all future (skip); else partial.
+GQA_HD int tile_class(int qs, int qe, int ks, int ke) {
+    if (ke <= qs) return kTileAllPast;
+    if (ks >= qe) return kTileAllFuture;
+    return kTilePartial;
+}
+
+}  // namespace gqa

@@ -1,0 +1,142 @@
+// Host runtime: status word, workspace cache, SM count, tensor-map encoding,
+// error strings. No kernels live here.
+
+#include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gqa_attn.h"
+#include "ptx.cuh"
+#include "runtime.cuh"
+
+namespace gqa {
+namespace {
+
+std::mutex g_mu;
+std::map<int, unsigned*> g_status;  // device -> status word
+std::map<int, int> g_sms;           // device -> SM count
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+}  // namespace
+
+unsigned* status_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_status.find(dev);
+    if (it != g_status.end()) return it->second;
+    unsigned* p = nullptr;
+    if (cudaMalloc(&p, sizeof(unsigned)) != cudaSuccess) return nullptr;
+    if (cudaMemset(p, 0, sizeof(unsigned)) != cudaSuccess) {
+        cudaFree(p);
+        return nullptr;
+    }
+    g_status[dev] = p;
+    return p;
+}
+
+int num_sms() {
+    const int dev = current_device();
+    if (dev < 0) return -1;
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    g_sms[dev] = n;
+    return n;
+}
+
+void* stream_workspace(cudaStream_t stream, size_t bytes) {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace& w = g_ws[{dev, stream}];
+    if (w.bytes >= bytes && w.ptr) return w.ptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+        return nullptr;
+    // Grow by at least 2x so a sequence of growing calls allocates O(log) times.
+    size_t want = bytes > 2 * w.bytes ? bytes : 2 * w.bytes;
+    if (w.ptr) {
+        if (cudaFreeAsync(w.ptr, stream) != cudaSuccess) return nullptr;
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, want, stream) != cudaSuccess) return nullptr;
+    w.ptr = p;
+    w.bytes = want;
+    return p;
+}
+
+cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                                uint64_t outer, uint32_t box_inner, uint32_t box_rows,
+                                CUtensorMapSwizzle swizzle) {
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                             cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return e != cudaSuccess ? e : cudaErrorSymbolNotFound;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    cuuint64_t dims[3] = {inner, rows, outer};
+    cuuint64_t strides[2] = {inner * 2, inner * rows * 2};  // bytes, dims 1 and 2
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace gqa
+
+extern "C" int gqa_attn_check(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GQA_ERR_CUDA;
+    unsigned* w = gqa::status_word();
+    if (!w) return GQA_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return GQA_ERR_CUDA;
+    if (v != 0 && cudaMemset(w, 0, sizeof(unsigned)) != cudaSuccess) return GQA_ERR_CUDA;
+    if (v & gqa::kStatusTimeout) return GQA_ERR_DEVICE_TIMEOUT;
+    if (v & gqa::kStatusBadSeqlen) return GQA_ERR_DEVICE_BAD_INPUT;
+    return GQA_OK;
+}
+
+extern "C" const char* gqa_attn_strerror(int code) {
+    switch (code) {
+        case GQA_OK: return "ok";
+        case GQA_ERR_INVALID_ARG: return "invalid argument";
+        case GQA_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, G <= 8)";
+        case GQA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+        case GQA_ERR_CUDA: return "CUDA runtime or driver error";
+        case GQA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
+        case GQA_ERR_WORKSPACE:
+            return "workspace too small, misaligned, or growth needed during stream capture";
+        case GQA_ERR_DEVICE_BAD_INPUT: return "a seqlen outside [0, S_max] was clamped";
+        default: return "unknown error code";
+    }
+}
+
+extern "C" int gqa_attn_version(void) { return 100; }

@@ -1,0 +1,173 @@
+/*
+ * gqa_attn.h — C ABI of the GB300 (sm_103a) grouped-query attention library.
+ *
+ * The operations are the ones defined on the page "ADR-0060: AHBM GQA Fused
+ * Attention kernel (Llama3-70B)" (kernbench2):
+ *   - decode: FlashDecoding split-KV sweep (§5.2 decode without sequence
+ *     parallelism, §3 per-tile op sequence) followed by the log-sum-exp merge
+ *     of the per-split partials (§4 reduction);
+ *   - prefill: FlashAttention tiled online softmax with causal tile skipping
+ *     and a boundary mask on partial tiles (§5.4 prefill without sequence
+ *     parallelism, §3).
+ * Both compute exactly O = softmax(Q K^T * scale + mask) V (the page's
+ * algorithm-lineage paragraph: no new mathematics) and lse = ln sum exp of the
+ * scaled, visible scores, per query row.
+ *
+ * Layouts (all row-major, contiguous, device memory unless stated):
+ *   q    decode  [B, H_q, d]          prefill [B, H_q, T_q, d]      bf16
+ *   k, v decode  [B, H_kv, S_max, d]  prefill [B, H_kv, S_kv, d]   bf16
+ *   o    like q                                                    bf16
+ *   lse  decode  [B, H_q]             prefill [B, H_q, T_q]        fp32
+ * bf16 values are passed as their 16-bit patterns (uint16_t).
+ * Query head h reads KV head h / G with G = H_q / H_kv: the G query heads of
+ * one KV head are adjacent (§0.5 I/O contract stores Q per KV head as
+ * [G, T_q, d]).
+ *
+ * Ownership: the caller owns every buffer passed in; the library never frees
+ * or retains a caller pointer after the call returns. All calls are
+ * asynchronous on `stream` (NULL = the legacy default stream) and do not
+ * synchronise. Inputs are read-only (§0.5 preconditions: Q and K are
+ * post-RoPE and the cache already holds the current token).
+ *
+ * Errors: every entry point returns 0 (GQA_OK) or a negative code and checks
+ * its arguments on the host before launching anything; an invalid argument
+ * never reaches the GPU. Errors the device detects (a bounded wait that ran
+ * out, a seqlen outside [0, S_max]) set a device status word that
+ * gqa_attn_check() reads.
+ */
+#ifndef GQA_ATTN_H_
+#define GQA_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* cudaStream_t;
+
+enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = -1,    /* null pointer, bad size, H_q % H_kv != 0, ... */
+    GQA_ERR_UNSUPPORTED = -2,    /* d not in {64, 128}, or G > 8 */
+    GQA_ERR_MISALIGNED = -3,     /* a tensor pointer is not 16-byte aligned */
+    GQA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
+    GQA_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (device status) */
+    GQA_ERR_WORKSPACE = -6,      /* caller workspace too small or misaligned */
+    GQA_ERR_DEVICE_BAD_INPUT = -7 /* the device saw a seqlen outside [0, S_max] */
+};
+
+/* ---------------------------------------------------------------- decode --
+ * gqa_attn_decode: one new query token per sequence (T_q = 1) against a KV
+ * cache of S_max slots, of which the first seqlens[b] are valid for row b
+ * (seqlens == NULL: all S_max). Page: §5.2 (decode, no SP) — every past key is
+ * visible, only the ragged tail is masked; G query heads are folded into the
+ * matmul M dimension so each K/V tile is read once per KV head.
+ *
+ * Split plan (§4 FlashDecoding split-and-combine; the page's round-robin
+ * rank placement has no counterpart on one GPU): num_splits contiguous
+ * chunks of L = ceil(S_max / num_splits) keys; split s of row b covers
+ * [min(s*L, seqlen_b), min((s+1)*L, seqlen_b)). num_splits <= 0 picks it
+ * with gqa_attn_pick_num_splits() for the current device.
+ *
+ *   q, k, v, o : see layouts above; 16-byte aligned.
+ *   lse        : [B, H_q] fp32, or NULL to skip it. A row with seqlen 0 gets
+ *                O = 0 and lse = -inf.
+ *   seqlens    : device int32 [B], or NULL. Values outside [0, S_max] are
+ *                clamped and reported as GQA_ERR_DEVICE_BAD_INPUT by
+ *                gqa_attn_check().
+ *   scale      : softmax scale (finite), usually 1/sqrt(d).
+ *   num_splits : 0 = automatic, else 1..8192.
+ * The workspace for the per-split partials is library-owned: one buffer per
+ * (device, stream), grown with stream-ordered allocation on first use. The
+ * first call on a stream should therefore happen before any stream capture.
+ * Calls on different streams never share a workspace.
+ */
+int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    uint16_t* o, float* lse, const int32_t* seqlens,
+                    int B, int H_q, int H_kv, int d, int S_max,
+                    float scale, int num_splits, cudaStream_t stream);
+
+/* The same, with a caller-provided device workspace (256-byte aligned) of at
+ * least gqa_attn_decode_workspace_size(B, H_q, d, num_splits) bytes; here
+ * num_splits must be >= 1 (resolve 0 with gqa_attn_pick_num_splits first).
+ * The workspace holds no state between calls; calls that overlap on the GPU
+ * must not share one. */
+int gqa_attn_decode_ws(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       uint16_t* o, float* lse, const int32_t* seqlens,
+                       int B, int H_q, int H_kv, int d, int S_max,
+                       float scale, int num_splits,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of decode workspace for these sizes (0 when num_splits == 1, which
+ * writes O directly). Returns 0 on invalid sizes as well. */
+size_t gqa_attn_decode_workspace_size(int B, int H_q, int d, int num_splits);
+
+/* --------------------------------------------------------------- prefill --
+ * gqa_attn_prefill: T_q new queries at global positions q_offset + t against
+ * S_kv keys (the cache already holds the new keys: q_offset + T_q <= S_kv).
+ * causal != 0: key j is visible to query t iff j <= q_offset + t; fully
+ * future KV tiles are skipped and partial tiles masked (§5.4). causal == 0:
+ * every key is visible. Fixed to the Llama3-70B head geometry of §0
+ * (H_q = 64, H_kv = 8, d = 128); gqa_attn_prefill_ex takes any supported one.
+ *   lse : [B, H_q, T_q] fp32, or NULL.
+ */
+int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     uint16_t* o, float* lse,
+                     int B, int T_q, int S_kv, int q_offset, int causal,
+                     float scale, cudaStream_t stream);
+
+int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        uint16_t* o, float* lse,
+                        int B, int H_q, int H_kv, int d, int T_q, int S_kv,
+                        int q_offset, int causal, float scale, cudaStream_t stream);
+
+/* ------------------------------------------------------ plan / scheduler --
+ * Integer helpers the kernels use, exported so tests can compare them with
+ * independent derivations bit for bit. Host-only; no GPU needed.
+ */
+
+/* Split count for a decode problem: enough (B * H_kv * num_splits) blocks to
+ * fill num_sms SMs, with at least 256 keys per split. Returns >= 1, or
+ * GQA_ERR_INVALID_ARG. */
+int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
+
+/* Fills starts[s], ends[s] (s < num_splits) with the decode split plan above
+ * for one row of length seqlen (0 <= seqlen <= S_max). */
+int gqa_attn_split_bounds(int S_max, int num_splits, int seqlen,
+                          int32_t* starts, int32_t* ends);
+
+/* §5.4 classification of query block [qs, qe) against KV tile [ks, ke), in
+ * global positions: 0 = all past (ke <= qs, no mask), 2 = all future
+ * (ks >= qe, skipped), 1 = partial (masked). */
+int gqa_attn_tile_class(int qs, int qe, int ks, int ke);
+
+/* Tile counts of the prefill kernel's own schedule for one (batch, head):
+ * query blocks of gqa_attn_prefill_block_m() rows, KV tiles of
+ * gqa_attn_prefill_block_n() keys, classified as above. Writes the number of
+ * all-past, partial and all-future (skipped) tile pairs. */
+int gqa_attn_prefill_tile_counts(int T_q, int S_kv, int q_offset, int causal,
+                                 int64_t* n_past, int64_t* n_partial, int64_t* n_future);
+int gqa_attn_prefill_block_m(void);
+int gqa_attn_prefill_block_n(void);
+
+/* ------------------------------------------------------------ status ----- */
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device. Returns GQA_OK, GQA_ERR_DEVICE_TIMEOUT,
+ * GQA_ERR_DEVICE_BAD_INPUT or GQA_ERR_CUDA. */
+int gqa_attn_check(cudaStream_t stream);
+
+/* Static, human-readable text for a return code. */
+const char* gqa_attn_strerror(int code);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int gqa_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H_ */

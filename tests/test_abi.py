@@ -1,0 +1,149 @@
+"""C ABI: the library loads, exports every declared symbol, its integer plan
+matches independent derivations bit for bit, and bad arguments come back as
+error codes before anything reaches a GPU. No GPU needed."""
+
+import ctypes
+import itertools
+import os
+import re
+
+import pytest
+
+import oracle as orc
+from gqa_attention_split_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return api.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_attn_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported_and_bound(L):
+    declared = _declared_functions()
+    assert "gqa_attn_decode" in declared and "gqa_attn_prefill" in declared
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(api.symbols()) == declared
+
+
+def test_version_and_strerror(L):
+    assert api.gqa_attn_version() >= 100
+    for code in range(0, -8, -1):
+        assert api.strerror(code) and api.strerror(code) != "unknown error code"
+    assert api.strerror(-99) == "unknown error code"
+
+
+def test_split_bounds_bit_exact_vs_oracle(L):
+    for S_max in (1, 2, 7, 64, 255, 256, 1000, 8192):
+        for ns in (1, 2, 3, 4, 7, 19, S_max):
+            for seqlen in sorted({0, 1, S_max // 3, S_max - 1, S_max}):
+                if seqlen < 0:
+                    continue
+                rc, got = api.gqa_attn_split_bounds(S_max, ns, seqlen)
+                assert rc == 0
+                assert got == orc.split_bounds(S_max, ns, seqlen), (S_max, ns, seqlen)
+
+
+def test_split_bounds_rejects_bad_args(L):
+    assert api.gqa_attn_split_bounds(10, 0, 5)[0] == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_split_bounds(10, 2, 11)[0] == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_split_bounds(10, 2, -1)[0] == api.GQA_ERR_INVALID_ARG
+
+
+def test_tile_class_bit_exact_vs_oracle(L):
+    for qs, qe, ks, ke in itertools.product(range(0, 7), range(1, 8), range(0, 7), range(1, 8)):
+        if qe > qs and ke > ks:
+            assert api.gqa_attn_tile_class(qs, qe, ks, ke) == orc.tile_class(qs, qe, ks, ke)
+
+
+@pytest.mark.parametrize("T_q,S_kv,off,causal", [(8192, 8192, 0, 1), (2048, 32768, 30720, 1),
+                                                 (300, 300, 0, 1), (17, 50, 33, 1),
+                                                 (1000, 1000, 0, 0), (0, 10, 0, 1)])
+def test_prefill_tile_counts_bit_exact_vs_oracle(L, T_q, S_kv, off, causal):
+    bm, bn = api.gqa_attn_prefill_block_m(), api.gqa_attn_prefill_block_n()
+    rc, past, part, fut = api.gqa_attn_prefill_tile_counts(T_q, S_kv, off, causal)
+    assert rc == 0
+    if T_q == 0:
+        assert past == part == fut == 0
+        return
+    cls = orc.prefill_tile_classes(T_q, S_kv, off, bm, bn)
+    if not causal:
+        assert (past, part, fut) == (cls.size, 0, 0)
+    else:
+        assert past == int((cls == orc.TILE_ALL_PAST).sum())
+        assert part == int((cls == orc.TILE_PARTIAL).sum())
+        assert fut == int((cls == orc.TILE_ALL_FUTURE).sum())
+
+
+def test_pick_num_splits_properties(L):
+    # cfg-shaped cases and a sweep: 1 <= ns <= max(1, S/256); fills the SMs when it can.
+    assert api.gqa_attn_pick_num_splits(1, 8, 8192, 152) == 19
+    for B, H_kv, S, sms in itertools.product((1, 2, 4, 64), (1, 8), (1, 255, 256, 8192, 131072),
+                                             (1, 148, 152)):
+        ns = api.gqa_attn_pick_num_splits(B, H_kv, S, sms)
+        assert 1 <= ns <= max(1, S // 256)
+        if S // 256 >= -(-sms // (B * H_kv)):
+            assert B * H_kv * ns >= sms
+    assert api.gqa_attn_pick_num_splits(0, 8, 8192, 152) == api.GQA_ERR_INVALID_ARG
+
+
+def test_workspace_size(L):
+    assert api.gqa_attn_decode_workspace_size(1, 64, 128, 1) == 0
+    n = api.gqa_attn_decode_workspace_size(1, 64, 128, 19)
+    assert n >= 64 * 19 * (128 + 2) * 4 and n % 256 == 0
+    assert api.gqa_attn_decode_workspace_size(1, 64, 96, 19) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case fails host checks first
+
+
+@pytest.mark.parametrize("args,code", [
+    # q,k,v,o null
+    ((0, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 0, 0, 0, 1, 8, 1, 64, 256, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    # H_q % H_kv != 0
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 6, 4, 64, 256, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    # bad sizes
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, -1, 8, 1, 64, 256, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 0, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, -2), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, float("nan"), 0), api.GQA_ERR_INVALID_ARG),
+    # unsupported head dim / group size
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 96, 256, 0.125, 0), api.GQA_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 16, 1, 64, 256, 0.125, 0), api.GQA_ERR_UNSUPPORTED),
+    # misaligned pointer
+    ((FAKE + 2, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, 0), api.GQA_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE + 8, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, 0), api.GQA_ERR_MISALIGNED),
+])
+def test_decode_bad_args_return_codes_without_launch(L, args, code):
+    assert api.gqa_attn_decode(*args, None) == code
+
+
+def test_decode_ws_rejects_auto_split_count(L):
+    rc = api.gqa_attn_decode_ws(FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, 0,
+                                FAKE, 1 << 20, None)
+    assert rc == api.GQA_ERR_INVALID_ARG
+
+
+def test_decode_empty_batch_is_a_no_op(L):
+    assert api.gqa_attn_decode(FAKE, FAKE, FAKE, FAKE, 0, 0, 0, 8, 1, 64, 256, 0.125, 0,
+                               None) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 1, 0.1), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 7, 128, 128, 128, 0, 1, 0.1), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, -1, 1, 0.1), api.GQA_ERR_INVALID_ARG),
+])
+def test_prefill_bad_args_return_codes_without_launch(L, args, code):
+    assert api.gqa_attn_prefill_ex(*args, None) == code
