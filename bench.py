@@ -1,0 +1,570 @@
+#!/usr/bin/env python3
+"""Benchmark of the GQA attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+
+One step = one decode token through the 80 attention layers of a Llama3-70B
+shaped model at S_kv = 8192 (B=1, H_q=64, H_kv=8, d=128 per layer; 80 KV
+caches, 2.7 GB resident in HBM, so L2 never holds a layer's cache between
+uses), replayed as one CUDA graph of 80 ``gqa_attn_decode`` calls, followed by
+one 8K causal prefill call (B=1, T_q=S_kv=8192; 335 MB of operands, larger than
+L2). ``value`` is decode KV GB/s; the prefill TFLOPS are in ``prefill``.
+
+For N > 1 (torchrun) every rank runs the same work on its own GPU with no
+data-path collective (weak scaling); a barrier and a max over ranks bracket
+the timed region. ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workloads instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% of 8 TB/s) & tok/s; prefill TFLOPS (% bf16 peak)"
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
+LAYERS = 80  # Llama3-70B decoder layers
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------- workloads
+
+
+def decode_bytes(B, H_q, H_kv, d, seqlens):
+    """Algorithmic bytes of one decode call: K and V rows read, q read, O and lse written."""
+    kv = 2 * H_kv * d * 2 * int(sum(seqlens))
+    return kv, kv + B * H_q * d * 2 * 2 + B * H_q * 4
+
+
+def prefill_flops(B, H_q, d, T_q, S_kv, q_offset, causal):
+    """4 * d flops per visible (query, key) pair (Q K^T and P V), visible pairs only."""
+    if causal:
+        pairs = sum(min(S_kv, q_offset + t + 1) for t in range(T_q))
+    else:
+        pairs = T_q * S_kv
+    return 4.0 * d * H_q * B * pairs
+
+
+def prefill_bytes(B, H_q, H_kv, d, T_q, S_kv):
+    return (2 * B * H_q * T_q * d * 2) + (2 * B * H_kv * S_kv * d * 2) + B * H_q * T_q * 4
+
+
+# ------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+
+def cpu_oracle_sample(seconds: float, steps: int = 1):
+    """Times the fp64 oracle, as it stands, on rows of the two workloads (one thread).
+
+    Runs in a fresh single-threaded process; each of `steps` samples spends about
+    `seconds` of CPU time. Returns one dict per step with decode GB/s (KV bytes of
+    whole decode calls, pro rata per query head) and prefill TFLOPS.
+    """
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(seconds),
+           "--cpu-worker-steps", str(steps)]
+    out = subprocess.run(cmd, env=env, capture_output=True, text=True,
+                         timeout=120 + 3 * seconds * steps)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_worker(seconds: float, steps: int):
+    import torch
+
+    torch.set_num_threads(1)
+    import oracle
+    from gqa_attention_split_gb300 import workloads as wl
+
+    w = wl.LLAMA70B_DECODE_8K
+    q, k, v, sl = wl.decode_inputs(w)
+    kv_bytes, _ = decode_bytes(w.B, w.H_q, w.H_kv, w.d, sl.tolist())
+    p = wl.CAUSAL_PREFILL_8K
+    qp, kp, vp = wl.prefill_inputs(p)
+    res = []
+    rows = n = 0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        r0 = rows
+        while time.perf_counter() - t0 < seconds / 2 or rows == r0:
+            oracle.attention_rows(q[:, :, None], k, v, [(0, rows % w.H_q, 0)], scale=w.scale,
+                                  seqlens=sl.tolist())
+            rows += 1
+        td = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        flops = 0.0
+        n0 = n
+        while time.perf_counter() - t0 < seconds / 2 or n == n0:
+            t = (n * 997) % p.T_q  # spread over the causal triangle
+            oracle.attention_rows(qp, kp, vp, [(0, (n * 13) % p.H_q, t)], scale=p.scale,
+                                  causal=True, q_offset=p.q_offset)
+            flops += 4.0 * p.d * min(p.S_kv, p.q_offset + t + 1)
+            n += 1
+        tp = time.perf_counter() - t0
+        res.append({"decode_gbs": kv_bytes * (rows - r0) / w.H_q / td / 1e9,
+                    "decode_rows": rows - r0, "decode_s": td,
+                    "prefill_tflops": flops / tp / 1e12, "prefill_rows": n - n0,
+                    "prefill_s": tp, "threads": 1})
+    print(json.dumps(res))
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def aggregate_max(values, device, world):
+    """Element-wise max over ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from gqa_attention_split_gb300 import api
+    from gqa_attention_split_gb300 import build as _build
+    from gqa_attention_split_gb300 import workloads as wl
+
+    _build.build()
+    api.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_kind = load_peaks()
+
+    # ---- decode: 80 layers of the Llama3-70B 8K decode shape
+    w = wl.LLAMA70B_DECODE_8K
+    q0, k0, v0, sl0 = wl.decode_inputs(w)
+    gen = torch.Generator(device=dev).manual_seed(w.seed * 1000 + rank)
+    qs = torch.empty((LAYERS,) + tuple(q0.shape), dtype=torch.bfloat16, device=dev)
+    ks = torch.empty((LAYERS,) + tuple(k0.shape), dtype=torch.bfloat16, device=dev)
+    vs = torch.empty_like(ks)
+    qs.copy_(torch.randn(qs.shape, generator=gen, device=dev).to(torch.bfloat16))
+    for L_ in range(LAYERS):  # layer by layer to bound the fp32 temporaries
+        ks[L_].copy_(torch.randn(k0.shape, generator=gen, device=dev).to(torch.bfloat16))
+        vs[L_].copy_(torch.randn(v0.shape, generator=gen, device=dev).to(torch.bfloat16))
+    qs[0].copy_(q0)
+    ks[0].copy_(k0)
+    vs[0].copy_(v0)
+    seqlens = sl0.to(dev)
+    os_ = torch.empty_like(qs)
+    lses = torch.empty((LAYERS, w.B, w.H_q), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ns = args.num_splits or api.gqa_attn_pick_num_splits(w.B, w.H_kv, w.S_max, sms)
+
+    def decode_layers():
+        for L_ in range(LAYERS):
+            api.decode(qs[L_], ks[L_], vs[L_], seqlens, num_splits=ns, out=os_[L_],
+                       lse=lses[L_])
+
+    with torch.cuda.stream(stream):
+        decode_layers()  # allocates the stream's workspace before capture
+    stream.synchronize()
+    api.check(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        decode_layers()
+    kv_b, alg_b = decode_bytes(w.B, w.H_q, w.H_kv, w.d, sl0.tolist())
+
+    # ---- prefill: one 8K causal call (if the kernel is in this build)
+    p = wl.CAUSAL_PREFILL_8K
+    qp, kp, vp = (t.to(dev) for t in wl.prefill_inputs(p))
+    op = torch.empty_like(qp)
+    lsep = torch.empty((p.B, p.H_q, p.T_q), dtype=torch.float32, device=dev)
+    have_prefill = True
+    try:
+        with torch.cuda.stream(stream):
+            api.prefill(qp, kp, vp, q_offset=p.q_offset, causal=True, out=op, lse=lsep)
+    except api.GqaError as e:
+        if e.code != api.GQA_ERR_UNSUPPORTED:
+            raise
+        have_prefill = False
+    pf_flops = prefill_flops(p.B, p.H_q, p.d, p.T_q, p.S_kv, p.q_offset, True)
+
+    def prefill_call():
+        api.prefill(qp, kp, vp, q_offset=p.q_offset, causal=True, out=op, lse=lsep)
+
+    splits_active = sum(math.ceil(int(s) / math.ceil(w.S_max / ns)) for s in sl0.tolist())
+    launches_decode = LAYERS * (1 + (1 if ns > 1 else 0))
+    launches_prefill = 1 if have_prefill else 0
+
+    def one_step(ev):
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            graph.replay()
+            ev[1].record(stream)
+            if have_prefill:
+                prefill_call()
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        one_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    stream.synchronize()
+    api.check(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first readings
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        one_step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    api.check(stream)
+
+    dec_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    pre_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    dec_ms, pre_ms, tot_ms = aggregate_max([dec_ms, pre_ms, dec_ms + pre_ms], dev, world)
+    K = args.steps
+    dec_call_s = dec_ms / 1e3 / (K * LAYERS)
+    dec_gbs_rank = kv_b / dec_call_s / 1e9
+    value = dec_gbs_rank * world  # every rank decodes its own batch (weak scaling)
+    pre_s = pre_ms / 1e3 / K if have_prefill else None
+    pre_tflops = pf_flops / pre_s / 1e12 if have_prefill else None
+
+    # ---- end to end through the same entry points, host buffers in pinned memory
+    e2e = run_e2e(api, torch, dev, stream, w, ns, p, have_prefill, args, world)
+
+    hbm_peak = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops_sustained"])
+    roof = {"bound": "hbm", "achieved": alg_b / dec_call_s / 1e9, "peak": hbm_peak,
+            "unit": "GB/s", "frac": alg_b / dec_call_s / 1e9 / hbm_peak,
+            "traffic": args.traffic,
+            "kernel": "gqa_attn_decode call (split_kernel + PDL combine_kernel), per layer",
+            "peak_kind": peak_kind}
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": tot_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic N(0,1) bf16, seeded; random KV caches (no trained weights)",
+        "config": {"workload": f"{LAYERS} x {w.name} decode (graph) + {p.name}",
+                   "decode": {"B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
+                              "S_kv": w.S_max, "layers": LAYERS, "num_splits": ns,
+                              "active_splits": splits_active},
+                   "prefill": {"B": p.B, "H_q": p.H_q, "H_kv": p.H_kv, "d": p.d,
+                               "T_q": p.T_q, "S_kv": p.S_kv, "causal": True},
+                   "l2": "inputs larger than L2: 80 distinct 33.5 MB KV caches per step; "
+                         "prefill operands 335 MB",
+                   "parallelism": f"replicas x{world}"},
+        "decode": {"kv_GBps": value, "pct_of_8TBps": 100 * dec_gbs_rank / NOMINAL_HBM_GBS,
+                   "pct_of_measured_hbm": 100 * dec_gbs_rank / hbm_peak,
+                   "us_per_layer_call": dec_call_s * 1e6,
+                   "tok_per_s_one_layer": w.B / dec_call_s,
+                   "tok_per_s_80_layers": w.B / (dec_call_s * LAYERS)},
+        "prefill": None if not have_prefill else {
+            "TFLOPS": pre_tflops * world, "ms_per_call": pre_s * 1e3,
+            "pct_of_nominal_2250": 100 * pre_tflops / NOMINAL_BF16_TFLOPS,
+            "pct_of_measured_bf16": 100 * pre_tflops / float(peaks["bf16_tflops"]),
+            "flops_per_call": pf_flops},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": K * (launches_decode + launches_prefill),
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if have_prefill:
+        res["roofline_prefill"] = {
+            "bound": "tensor", "achieved": pre_tflops, "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": pre_tflops / tc_peak, "traffic": None, "kernel": "prefill_kernel",
+            "peak_kind": peak_kind + " sustained"}
+    return res
+
+
+def run_e2e(api, torch, dev, stream, w, ns, p, have_prefill, args, world):
+    """Same metric through the public API with pinned host inputs/outputs (one layer/call)."""
+    from gqa_attention_split_gb300 import workloads as wl
+
+    q, k, v, sl = wl.decode_inputs(w)
+    hq, hk, hv, hs = (t.pin_memory() for t in (q, k, v, sl))
+    dq, dk, dv, ds = (torch.empty_like(t, device=dev) for t in (q, k, v, sl))
+    ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.B, w.H_q), dtype=torch.float32).pin_memory()
+    do = torch.empty_like(dq)
+    dl = torch.empty((w.B, w.H_q), dtype=torch.float32, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs))
+    d2h = ho.numel() * 2 + hl.numel() * 4
+    kv_b, _ = decode_bytes(w.B, w.H_q, w.H_kv, w.d, sl.tolist())
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        for src, dst in ((hq, dq), (hk, dk), (hv, dv), (hs, ds)):
+            dst.copy_(src, non_blocking=True)
+        api.decode(dq, dk, dv, ds, num_splits=ns, out=do, lse=dl)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    out = {"value": kv_b / t / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "what": f"one {w.name} decode call per step"}
+    if have_prefill:
+        qp, kp, vp = wl.prefill_inputs(p)
+        hqp, hkp, hvp = (x.pin_memory() for x in (qp, kp, vp))
+        dqp, dkp, dvp = (torch.empty_like(x, device=dev) for x in (qp, kp, vp))
+        hop = torch.empty(qp.shape, dtype=torch.bfloat16).pin_memory()
+        hlp = torch.empty((p.B, p.H_q, p.T_q), dtype=torch.float32).pin_memory()
+        dop = torch.empty_like(dqp)
+        dlp = torch.empty((p.B, p.H_q, p.T_q), dtype=torch.float32, device=dev)
+
+        def pstep():
+            for src, dst in ((hqp, dqp), (hkp, dkp), (hvp, dvp)):
+                dst.copy_(src, non_blocking=True)
+            api.prefill(dqp, dkp, dvp, q_offset=p.q_offset, causal=True, out=dop, lse=dlp)
+            hop.copy_(dop, non_blocking=True)
+            hlp.copy_(dlp, non_blocking=True)
+
+        psteps = max(3, min(args.steps, 10))
+        with torch.cuda.stream(stream):
+            pstep()
+            stream.synchronize()
+            e0.record(stream)
+            for _ in range(psteps):
+                pstep()
+            e1.record(stream)
+        stream.synchronize()
+        tp = e0.elapsed_time(e1) / 1e3 / psteps
+        flops = prefill_flops(p.B, p.H_q, p.d, p.T_q, p.S_kv, p.q_offset, True)
+        out["prefill"] = {"value": flops / tp / 1e12 * world, "unit": "TFLOP/s",
+                          "h2d_bytes_per_step": sum(x.numel() * 2 for x in (qp, kp, vp)),
+                          "d2h_bytes_per_step": hop.numel() * 2 + hlp.numel() * 4}
+    return out
+
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle as the reference arm, on this arm's config and metric."""
+    if rank != 0:
+        return None
+    # The whole run stays within a few minutes: about 150 s of CPU work in total.
+    per = max(0.2, min(args.ref_seconds, 150.0 / (args.warmup + args.steps)))
+    per_step = cpu_oracle_sample(per, args.warmup + args.steps)
+    timed = per_step[args.warmup:]
+    info = timed[-1]
+    dec = statistics.mean(x["decode_gbs"] for x in timed)
+    pre = statistics.mean(x["prefill_tflops"] for x in timed)
+    sample = (f"per step: {info['decode_rows']} query-head rows of the 8K decode "
+              f"({info['decode_s']:.1f}s) and {info['prefill_rows']} rows of the 8K causal "
+              f"prefill ({info['prefill_s']:.1f}s), fp64 oracle, 1 thread")
+    return {"impl": "reference", "metric": METRIC, "value": dec, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(x["decode_s"] + x["prefill_s"] for x in timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic N(0,1) bf16 widened to fp64, seeded",
+            "config": {"workload": f"{LAYERS} x llama70b_decode_b1_s8192 decode (graph) + "
+                                   "llama70b_causal_prefill_b1_t8192"},
+            "prefill": {"TFLOPS": pre},
+            "cpu_baseline": {"value": dec, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": dec, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_case(args):
+    """One workload alone, plain launches (no graph): for profiling and quick timing."""
+    import torch
+
+    from gqa_attention_split_gb300 import api
+    from gqa_attention_split_gb300 import build as _build
+    from gqa_attention_split_gb300 import workloads as wl
+
+    _build.build()
+    api.lib()
+    dev = torch.device("cuda", 0)
+    if args.case in ("decode8k", "ragged128k"):
+        w = wl.LLAMA70B_DECODE_8K if args.case == "decode8k" else wl.RAGGED_DECODE_128K
+        q, k, v, sl = (t.to(dev) for t in wl.decode_inputs(w))
+        kv_b, _ = decode_bytes(w.B, w.H_q, w.H_kv, w.d, sl.tolist())
+
+        def call():
+            api.decode(q, k, v, sl, num_splits=args.num_splits)
+
+        work, unit = kv_b / 1e9, "GB/s"
+    elif args.case in ("prefill8k", "chunked32k"):
+        p = wl.CAUSAL_PREFILL_8K if args.case == "prefill8k" else wl.CHUNKED_PREFILL_32K
+        q, k, v = (t.to(dev) for t in wl.prefill_inputs(p))
+
+        def call():
+            api.prefill(q, k, v, q_offset=p.q_offset, causal=True)
+
+        work = prefill_flops(p.B, p.H_q, p.d, p.T_q, p.S_kv, p.q_offset, True) / 1e12
+        unit = "TFLOP/s"
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    api.check()
+    times = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    api.check()
+    med = statistics.median(times)
+    print(json.dumps({"case": args.case, "median_us": med * 1e6, "value": work / med,
+                      "unit": unit, "steps": args.steps,
+                      "note": "plain launches, warm L2 possible; not a bench value"}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work for the cpu_baseline leg")
+    ap.add_argument("--ref-seconds", type=float, default=4.0,
+                    help="CPU work per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per decode call, if captured for this build")
+    ap.add_argument("--case", default=None,
+                    help="decode8k | ragged128k | prefill8k | chunked32k: one workload alone")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-worker-steps", type=int, default=1, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.cpu_worker is not None:
+        cpu_worker(args.cpu_worker, args.cpu_worker_steps)
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.case:
+        run_case(args)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            cb = cpu_oracle_sample(args.cpu_seconds)[0]
+            res["cpu_baseline"] = {
+                "value": cb["decode_gbs"], "unit": "GB/s", "cores": cb["threads"],
+                "kind": "oracle",
+                "sample": f"{cb['decode_rows']} query-head rows of the 8K decode in "
+                          f"{cb['decode_s']:.1f}s (fp64 oracle, 1 thread); prefill rows: "
+                          f"{cb['prefill_tflops']:.2e} TFLOP/s over {cb['prefill_rows']} rows",
+                "prefill_TFLOPS": cb["prefill_tflops"]}
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -52,7 +52,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, src + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        extra = os.environ.get("GQA_EXTRA_NVCC_FLAGS", "").split()
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_verbose and src.endswith(".cu"):
             cmd.insert(1, "-Xptxas=-v")
         if verbose:

@@ -1,5 +1,5 @@
-// Split-KV GQA decode for sm_103a: a KV-bandwidth-bound sweep that writes
-// per-split (m, l, O) partials, and a log-sum-exp combine.
+// Split-KV GQA decode for sm_103a: a KV-bandwidth-bound sweep over key
+// splits, merged with the log-sum-exp rule in two levels.
 //
 // Page: "ADR-0060: AHBM GQA Fused Attention kernel (Llama3-70B)".
 //   §5.2 decode, no SP: T_q = 1, the G query heads of one KV head are folded
@@ -8,31 +8,43 @@
 //   §3 per-tile op sequence: S_j = q_g K_j^T * scale, m_new = max(m, rowmax),
 //        P = exp(S_j - m_new), corr = exp(m - m_new), l = l*corr + rowsum P,
 //        O = O*corr + P V_j.
-//   §4 reduction: the split partials merge with the log-sum-exp rule and are
-//        normalised once (here: by the combine kernel, in split order).
+//   §4 reduction: partials (m, l, O) merge with the log-sum-exp rule as a
+//        2-level reduce-to-root (level 2 inside a CUBE, level 1 across the
+//        CUBE group), normalised once at the root.
 //
-// GB300 mapping. One CTA per (split, KV head, batch row). Each warp owns an
-// independent ring of STAGES shared-memory stages, each holding TILE_T keys
-// of K and V, filled by TMA (128-byte swizzle, so the ldmatrix reads below
-// are bank-conflict free). Warps take the split's tiles round-robin. The
-// tensor-core work runs "swapped": S^T = K_j q^T (M = 16 keys, N = 8 query
-// heads) and O^T += V_j^T P^T (M = 16 dims, N = 8 heads), so the 8 heads of a
-// group fill the N = 8 side of mma.m16n8k16 with no padding; P^T moves from
-// the accumulator layout to the B-operand layout with movmatrix. The
-// exponentials run in base 2 with the scale folded into log2(e)*scale.
-// Warps merge their partials in shared memory in fixed order, so results
-// are deterministic. A split's last, ragged tile is loaded shifted back to
-// end at the split's last key, so every row TMA brings in holds either a
-// real cache entry of this row or zero fill; keys outside the tile's own
-// range are masked by selection (-inf), never by arithmetic on garbage.
+// GB300 mapping.
+// * One CTA per (split, KV head, batch row). Each warp owns a ring of STAGES
+//   shared-memory stages of TILE_T keys of K and V, filled by TMA with
+//   128-byte swizzle (bank-conflict-free ldmatrix). Warps take the split's
+//   tiles round-robin.
+// * Tensor cores run "swapped": S^T = K_j q^T (M = 16 keys, N = 8 query heads)
+//   and O^T += V_j^T P^T (M = 16 dims, N = 8 heads), so the 8 heads of a group
+//   fill the N = 8 side of mma.m16n8k16; movmatrix turns the P^T accumulator
+//   into the B operand. Exponentials run in base 2 with log2(e)*scale folded
+//   into the scores.
+// * Level 2 of the reduction: the warps of a CTA merge in shared memory, then
+//   the CS CTAs of a thread-block cluster (consecutive splits of one KV head)
+//   merge through distributed shared memory, in cluster-rank order. If one
+//   cluster spans the whole row it writes O and lse directly.
+// * Level 1 (only when a row spans several clusters): each cluster writes a
+//   partial to the workspace and a PDL-launched combine kernel merges them in
+//   group order.
+// * A split's last, ragged tile is loaded shifted back to end at the split's
+//   last key, so every row TMA brings in is a real cache entry of this row or
+//   zero fill; keys outside the tile's own range are masked by selection
+//   (-inf), never by arithmetic on padding.
+// All merges use a fixed order, so results are bitwise deterministic.
 
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "gqa_attn.h"
 #include "plan.cuh"
 #include "ptx.cuh"
 #include "runtime.cuh"
+#include "trace.cuh"
 
 namespace gqa {
 namespace decode {
@@ -44,28 +56,39 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct SplitParams {
     const uint16_t* q;        // [B, H_q, D]
     const int32_t* seqlens;   // [B] or null
-    uint16_t* o;              // [B, H_q, D]   (written when ns == 1)
-    float* lse;               // [B, H_q] or null (written when ns == 1)
-    float* part_o;            // [B, H_q, ns, D]  unnormalised
-    float* part_m;            // [B, H_q, ns]     base-2 running max
-    float* part_l;            // [B, H_q, ns]
+    uint16_t* o;              // [B, H_q, D]   (written when n_groups == 1)
+    float* lse;               // [B, H_q] or null
+    float* part_o;            // [B, H_q, n_groups, D]  unnormalised group partials
+    float* part_m;            // [B, H_q, n_groups]     base-2 running max
+    float* part_l;            // [B, H_q, n_groups]
     unsigned* status;
-    int B, H_q, H_kv, G, S_max, ns, L;
+    int B, H_q, H_kv, G, S_max, ns, L, n_groups;
     float scale_log2;         // scale * log2(e)
 };
 
 template <int D, int TILE_T, int STAGES, int WARPS>
 struct SplitCfg {
+    static constexpr int kThreads = WARPS * 32;
     static constexpr int kBoxes = D / 64;               // 128-byte column boxes per row
     static constexpr int kBoxBytes = TILE_T * 128;      // one box: TILE_T rows x 128 B
     static constexpr int kKBytes = kBoxes * kBoxBytes;  // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kRingBytes = WARPS * STAGES * kStageBytes;
-    static constexpr int kOPitch = D + 4;               // floats; breaks bank conflicts
-    static constexpr int kMergeBytes = WARPS * kMaxG * (kOPitch + 2) * 4;
+    // Per-head record a CTA sends to the head's owner in the cluster:
+    // {m, l, 0, 0, O[0..D)} as floats (16 + 4*D bytes, a multiple of 16).
+    static constexpr int kRec = 4 + D;
+    static constexpr int kRecBytes = kRec * 4;
+    static constexpr int kWarpMergeFloats = (WARPS - 1) * (D / 16 * 4 + 4) * 32;
+    static constexpr int kSendFloats = kMaxG * kRec;
+    static constexpr int kMergeBytes = (kSendFloats + kWarpMergeFloats) * 4;
     static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
-    static constexpr int kBarOffset = kDataBytes;
-    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kDataBytes + WARPS * STAGES * 8;
+    // Inbound records: [heads per rank][CS][kRec]. A rank owns ceil(8 / CS)
+    // heads, so it receives at most 16 records for any CS <= 16.
+    static constexpr int kRecvOffset = kDataBytes;
+    static constexpr int kRecvBytes = 2 * kMaxG * kRecBytes;
+    static constexpr int kBarOffset = kRecvOffset + kRecvBytes;
+    static constexpr int kSmemBytes =
+        1024 /*alignment slack*/ + kBarOffset + (WARPS * STAGES + 1) * 8;
     static constexpr int kMT = TILE_T / 16;             // 16-key m-tiles per stage
     static constexpr int kKC = D / 16;                  // 16-wide k-chunks of a head dim
     static_assert(TILE_T % 16 == 0 && TILE_T <= 256, "tile");
@@ -89,53 +112,108 @@ __device__ __forceinline__ int load_seqlen(const int32_t* seqlens, int b, int S_
     return sl;
 }
 
-template <int D, int TILE_T, int STAGES, int WARPS>
+__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Writes one merged (m, l, O) element: the final normalised output when the
+// row has a single group, else the group's partial for the combine kernel.
+__device__ __forceinline__ void emit(const SplitParams& p, size_t row, int gi, int dim, int D,
+                                     float m, float l, float o) {
+    if (p.n_groups == 1) {
+        p.o[row * D + dim] = to_bf16_bits(l > 0.f ? o / l : 0.f);
+        if (dim == 0 && p.lse) p.lse[row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    } else {
+        const size_t pr = row * p.n_groups + gi;
+        p.part_o[pr * D + dim] = o;
+        if (dim == 0) {
+            p.part_m[pr] = m;
+            p.part_l[pr] = l;
+        }
+    }
+}
+
+template <int D, int TILE_T, int STAGES, int WARPS, int CS>
 __global__ void __launch_bounds__(WARPS * 32, 1)
     split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const SplitParams p) {
     using C = SplitCfg<D, TILE_T, STAGES, WARPS>;
     const int s = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+    const int gi = s / CS;         // cluster (group) index within the row
+    const int rank = s % CS;       // == %cluster_ctarank for a (CS, 1, 1) cluster
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
 
-    // Let the combine grid get scheduled while this one streams (it waits
-    // for our results with griddepcontrol.wait before reading anything).
+    // Let a dependent combine grid get scheduled while this one streams (it
+    // waits for our results with griddepcontrol.wait before reading anything).
     pdl_launch_dependents();
-
-    const int seqlen = load_seqlen(p.seqlens, b, p.S_max, p.status,
-                                   s == 0 && kv == 0 && threadIdx.x == 0);
-    const SplitRange r = split_range(p.L, s, seqlen);
-    if (r.end <= r.start) {
-        // Empty split. The combine skips it; with a single split this block
-        // owns the output: a row with no visible keys gives O = 0, lse = -inf.
-        if (p.ns == 1) {
-            for (int i = threadIdx.x; i < p.G * D; i += WARPS * 32) {
-                const int h = kv * p.G + i / D;
-                p.o[(size_t(b) * p.H_q + h) * D + i % D] = 0;
-                if (i % D == 0 && p.lse) p.lse[size_t(b) * p.H_q + h] = -INFINITY;
-            }
-        }
-        return;
+    [[maybe_unused]] const int blin = (b * gridDim.y + kv) * gridDim.x + s;
+    if (threadIdx.x == 0) {
+        GQA_TRACE_STAMP(blin, 0);
+        unsigned smid;
+        asm("mov.u32 %0, %%smid;" : "=r"(smid));
+        GQA_TRACE_VALUE(blin, 5, smid);
     }
 
+    // ---- set-up that touches no global memory: it may overlap the previous
+    // kernel in the stream (programmatic dependent launch).
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset) + warp * STAGES;
     uint8_t* ring = smem + size_t(warp) * STAGES * C::kStageBytes;
-
-    const int len = r.end - r.start;
-    const int n_tiles = (len + TILE_T - 1) / TILE_T;
-    const int my_n = warp < n_tiles ? (n_tiles - warp + WARPS - 1) / WARPS : 0;
-    const int zc = b * p.H_kv + kv;  // outer TMA coordinate: (batch, KV head)
-
+    // Heads whose cluster merge this CTA owns: h = rank, rank + CS, ... < G.
+    const int n_own = CS > 1 && rank < p.G ? (p.G - rank + CS - 1) / CS : 0;
+    uint64_t* recv_bar = reinterpret_cast<uint64_t*>(smem + C::kBarOffset) + WARPS * STAGES;
+    float* recv = reinterpret_cast<float*>(smem + C::kRecvOffset);  // [n_own][CS][kRec]
     if (lane == 0) {
         for (int i = 0; i < STAGES; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        if (CS > 1 && warp == 0) {
+            // Armed before any peer can send: the peers' records complete it.
+            mbar_init(smem_u32(recv_bar), 1);
+            if (n_own > 0) mbar_arrive_expect_tx(smem_u32(recv_bar), n_own * CS * C::kRecBytes);
+        }
         fence_mbar_init();
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
     }
     __syncwarp();
+    // Cluster: publish the armed barrier now; wait for the peers' only before
+    // sending to them (by then every CTA has long passed this point).
+    if constexpr (CS > 1) cluster_arrive_release();
+
+    pdl_wait_primary();  // everything below may read what earlier kernels wrote
+
+    const int seqlen = load_seqlen(p.seqlens, b, p.S_max, p.status,
+                                   s == 0 && kv == 0 && threadIdx.x == 0);
+    // A whole group beyond the row's end does nothing (uniform over the
+    // cluster, so no CTA waits at a cluster barrier for one that left). With a
+    // single group this can only be a row of length 0: O = 0, lse = -inf.
+    if (int64_t(gi) * CS * p.L >= seqlen) {
+        if (p.n_groups == 1 && rank == 0) {
+            for (int i = threadIdx.x; i < p.G * D; i += C::kThreads) {
+                const size_t row = size_t(b) * p.H_q + kv * p.G + i / D;
+                emit(p, row, 0, i % D, D, -INFINITY, 0.f, 0.f);
+            }
+        }
+        return;
+    }
+    const SplitRange r = s < p.ns ? split_range(p.L, s, seqlen) : SplitRange{seqlen, seqlen};
+    const int len = r.end - r.start;
+    const int n_tiles = (len + TILE_T - 1) / TILE_T;
+    const int my_n = warp < n_tiles ? (n_tiles - warp + WARPS - 1) / WARPS : 0;
+    const int zc = b * p.H_kv + kv;  // outer TMA coordinate: (batch, KV head)
 
     const uint64_t policy = l2_policy_evict_first();
     // Row of the first key TMA brings in for this warp's i-th tile.
@@ -188,6 +266,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         const int slot = i % STAGES;
         if (alive) alive = mbar_wait_bounded(smem_u32(&bars[slot]), (i / STAGES) & 1, p.status);
         alive = __all_sync(0xffffffffu, alive);  // keep the warp's control flow uniform
+        if (i == 0 && threadIdx.x == 0) GQA_TRACE_STAMP(blin, 1);
         waited = i + 1;
         const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
@@ -270,9 +349,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
 
         __syncwarp();
-        if (lane == 0 && alive && issued < my_n) {
-            issue(issued);
-        }
+        if (lane == 0 && alive && issued < my_n) issue(issued);
         if (alive && issued < my_n) ++issued;
     }
     // A wait that ran out may leave copies in flight: wait for them (bounded)
@@ -285,55 +362,143 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 2);
 
-    // ---- merge the warps' partials in shared memory, warp order fixed
+    // ---- level 2a: the other warps hand their partials to warp 0, which
+    // merges them fragment by fragment in registers (warp order fixed).
+    constexpr int kFrag = C::kKC * 4 + 4;  // accumulators, then m0, m1, l0, l1
+    float* wbuf = reinterpret_cast<float*>(smem);  // [WARPS-1][kFrag][32]
+    float* rec = wbuf + C::kWarpMergeFloats;       // [8][kRec] records to send (clusters)
     __syncthreads();  // every warp is done with its ring
-    float* o_s = reinterpret_cast<float*>(smem);                  // [WARPS][8][kOPitch]
-    float* m_s = o_s + WARPS * kMaxG * C::kOPitch;                // [WARPS][8]
-    float* l_s = m_s + WARPS * kMaxG;                             // [WARPS][8]
-    if (g == 0) {
-        m_s[warp * kMaxG + 2 * c] = m0;
-        m_s[warp * kMaxG + 2 * c + 1] = m1;
-        l_s[warp * kMaxG + 2 * c] = l0;
-        l_s[warp * kMaxG + 2 * c + 1] = l1;
-    }
+    if (warp > 0) {
+        float* dst = wbuf + (warp - 1) * kFrag * 32 + lane;
 #pragma unroll
-    for (int md = 0; md < C::kKC; ++md) {
+        for (int md = 0; md < C::kKC; ++md)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int dim = md * 16 + g + (e >> 1) * 8;
-            const int head = 2 * c + (e & 1);
-            o_s[(warp * kMaxG + head) * C::kOPitch + dim] = acc[md][e];
-        }
+            for (int e = 0; e < 4; ++e) dst[(md * 4 + e) * 32] = acc[md][e];
+        dst[(C::kKC * 4 + 0) * 32] = m0;
+        dst[(C::kKC * 4 + 1) * 32] = m1;
+        dst[(C::kKC * 4 + 2) * 32] = l0;
+        dst[(C::kKC * 4 + 3) * 32] = l1;
     }
     __syncthreads();
-
-    for (int i = threadIdx.x; i < p.G * D; i += WARPS * 32) {
-        const int head = i / D, dim = i % D;
-        float mstar = -INFINITY;
+    if (warp == 0) {
+        float ms0 = m0, ms1 = m1;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) mstar = fmaxf(mstar, m_s[w * kMaxG + head]);
-        float lsum = 0.f, osum = 0.f;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w) {
-            const float f = fast_exp2(m_s[w * kMaxG + head] - mstar);
-            lsum += f * l_s[w * kMaxG + head];
-            osum += f * o_s[(w * kMaxG + head) * C::kOPitch + dim];
+        for (int w = 1; w < WARPS; ++w) {
+            const float* src = wbuf + (w - 1) * kFrag * 32 + lane;
+            ms0 = fmaxf(ms0, src[(C::kKC * 4 + 0) * 32]);
+            ms1 = fmaxf(ms1, src[(C::kKC * 4 + 1) * 32]);
         }
-        const size_t row = size_t(b) * p.H_q + kv * p.G + head;
-        if (p.ns == 1) {
-            const float out = osum / lsum;
-            p.o[row * D + dim] = __bfloat16_as_ushort(__float2bfloat16_rn(out));
-            if (dim == 0 && p.lse) p.lse[row] = (mstar + __log2f(lsum)) * kLn2;
-        } else {
-            const size_t pr = row * p.ns + s;
-            p.part_o[pr * D + dim] = osum;
-            if (dim == 0) {
-                p.part_m[pr] = mstar;
-                p.part_l[pr] = lsum;
+        // An empty CTA keeps (-inf, 0, 0); -inf - -inf never reaches exp2.
+        auto weight = [](float m, float mstar) {
+            return m == -INFINITY ? 0.f : fast_exp2(m - mstar);
+        };
+        const float f0 = weight(m0, ms0), f1 = weight(m1, ms1);
+        l0 *= f0;
+        l1 *= f1;
+#pragma unroll
+        for (int md = 0; md < C::kKC; ++md) {
+            acc[md][0] *= f0;
+            acc[md][1] *= f1;
+            acc[md][2] *= f0;
+            acc[md][3] *= f1;
+        }
+#pragma unroll
+        for (int w = 1; w < WARPS; ++w) {
+            const float* src = wbuf + (w - 1) * kFrag * 32 + lane;
+            const float g0 = weight(src[(C::kKC * 4 + 0) * 32], ms0);
+            const float g1 = weight(src[(C::kKC * 4 + 1) * 32], ms1);
+            l0 += g0 * src[(C::kKC * 4 + 2) * 32];
+            l1 += g1 * src[(C::kKC * 4 + 3) * 32];
+#pragma unroll
+            for (int md = 0; md < C::kKC; ++md) {
+                acc[md][0] += g0 * src[(md * 4 + 0) * 32];
+                acc[md][1] += g1 * src[(md * 4 + 1) * 32];
+                acc[md][2] += g0 * src[(md * 4 + 2) * 32];
+                acc[md][3] += g1 * src[(md * 4 + 3) * 32];
             }
         }
+        // Warp 0 now holds the CTA partial: lane (g, c) has heads 2c, 2c+1 at
+        // dims md*16 + g (+8).
+#pragma unroll
+        for (int md = 0; md < C::kKC; ++md) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int dim = md * 16 + g + (e >> 1) * 8;
+                const int head = 2 * c + (e & 1);
+                const float mm = (e & 1) ? ms1 : ms0, ll = (e & 1) ? l1 : l0;
+                if constexpr (CS == 1) {
+                    if (head < p.G)
+                        emit(p, size_t(b) * p.H_q + kv * p.G + head, gi, dim, D, mm, ll,
+                             acc[md][e]);
+                } else {
+                    rec[head * C::kRec + 4 + dim] = acc[md][e];
+                }
+            }
+        }
+        if (CS > 1 && g == 0) {
+            rec[(2 * c) * C::kRec + 0] = ms0;
+            rec[(2 * c) * C::kRec + 1] = l0;
+            rec[(2 * c + 1) * C::kRec + 0] = ms1;
+            rec[(2 * c + 1) * C::kRec + 1] = l1;
+        }
+        if constexpr (CS > 1) fence_proxy_async_smem();  // records -> async proxy
+        __syncwarp();
     }
+
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 4);
+    if constexpr (CS > 1) {
+        // ---- level 2b: push head h's record to its owner, rank h % CS, which
+        // merges the CS records of each head it owns in rank order.
+        cluster_wait_acquire();  // every peer's receive barrier is armed
+        if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 6);
+        if (warp == 0 && lane < p.G) {
+            const int h = lane, owner = h % CS;
+            const uint32_t src = smem_u32(rec + h * C::kRec);
+            const uint32_t dst = smem_u32(recv + ((h / CS) * CS + rank) * C::kRec);
+            bulk_copy_to_peer(map_to_rank(dst, owner), src, C::kRecBytes,
+                              map_to_rank(smem_u32(recv_bar), owner));
+            bulk_commit();
+        }
+        bool got = true;
+        if (n_own > 0) got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(recv_bar), 0,
+                                                                         p.status));
+        if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 7);
+        // Per owned head, warp 0 alone: lane q holds sender q's (m, l), the
+        // weights come from two warp reductions, and each lane folds the CS
+        // records over its D/32 dims with vector loads.
+        if (got && warp == 0) {
+            constexpr int kPer = D / 32;
+            using VecT = typename std::conditional<kPer == 4, float4, float2>::type;
+            for (int j = 0; j < n_own; ++j) {
+                const float* r0 = recv + j * CS * C::kRec;
+                const float mq = lane < CS ? r0[lane * C::kRec + 0] : -INFINITY;
+                const float lq = lane < CS ? r0[lane * C::kRec + 1] : 0.f;
+                const float mstar = warp_max(mq);
+                const float f = mq == -INFINITY ? 0.f : fast_exp2(mq - mstar);
+                const float lsum = warp_sum(f * lq);
+                float o[kPer];
+#pragma unroll
+                for (int e = 0; e < kPer; ++e) o[e] = 0.f;
+#pragma unroll
+                for (int q2 = 0; q2 < CS; ++q2) {
+                    const VecT v =
+                        *reinterpret_cast<const VecT*>(r0 + q2 * C::kRec + 4 + lane * kPer);
+                    const float fq = __shfl_sync(0xffffffffu, f, q2);
+                    const float* fv = reinterpret_cast<const float*>(&v);
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e) o[e] += fq * fv[e];
+                }
+                const size_t row = size_t(b) * p.H_q + kv * p.G + rank + j * CS;
+#pragma unroll
+                for (int e = 0; e < kPer; ++e) emit(p, row, gi, lane * kPer + e, D, mstar, lsum, o[e]);
+            }
+        }
+        // Our records must be read out before this CTA's shared memory goes away.
+        if (warp == 0 && lane < p.G) bulk_wait_read_all();
+    }
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 3);
 }
 
 struct CombineParams {
@@ -343,25 +508,34 @@ struct CombineParams {
     const int32_t* seqlens;
     uint16_t* o;
     float* lse;
-    int B, H_q, S_max, ns, L;
+    int B, H_q, S_max, n_groups;
+    int64_t group_len;  // keys per group: cluster size * L
 };
 
 constexpr int kCombineWarps = 8;
+[[maybe_unused]] constexpr int kTraceCombineBase = 60000;  // trace rows of combine blocks
 
-// One warp per (batch, query head): fold the row's non-empty splits in order
-// s = 0, 1, ... with the log-sum-exp rule, normalise once, write O and lse.
+// Level 1 of the reduction. One warp per (batch, query head): merge the row's
+// non-empty group partials with the log-sum-exp rule, normalise once, write O
+// and lse. Lane j holds group j's (m, l); the O partials of up to 8 groups are
+// loaded together so one L2 round trip serves them. The arithmetic order
+// depends only on the group count: results are deterministic.
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const CombineParams p) {
     constexpr int kPer = D / 32;  // dims per lane
+    using VecT = typename std::conditional<kPer == 4, float4, float2>::type;
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(kTraceCombineBase + blockIdx.x, 0);
+    pdl_launch_dependents();      // the next kernel may start its own set-up
     pdl_wait_primary();           // the split grid's partials are complete and visible
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(kTraceCombineBase + blockIdx.x, 1);
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     if (row >= p.B * p.H_q) return;
     const int b = row / p.H_q;
     int seqlen = p.seqlens ? p.seqlens[b] : p.S_max;
     seqlen = seqlen < 0 ? 0 : (seqlen > p.S_max ? p.S_max : seqlen);
-    const int n_act = active_splits(p.L, seqlen);
+    const int n_act = int((seqlen + p.group_len - 1) / p.group_len);
     float* out_lse = p.lse ? p.lse + row : nullptr;
     uint16_t* out = p.o + size_t(row) * D + lane * kPer;
     if (n_act == 0) {
@@ -370,44 +544,69 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
         if (lane == 0 && out_lse) *out_lse = -INFINITY;
         return;
     }
-    const float* pm = p.part_m + size_t(row) * p.ns;
-    const float* pl = p.part_l + size_t(row) * p.ns;
-    const float* po = p.part_o + size_t(row) * p.ns * D + lane * kPer;
+    const float* pm = p.part_m + size_t(row) * p.n_groups;
+    const float* pl = p.part_l + size_t(row) * p.n_groups;
+    const float* po = p.part_o + size_t(row) * p.n_groups * D + lane * kPer;
     float mx = -INFINITY;
     for (int s = lane; s < n_act; s += 32) mx = fmaxf(mx, pm[s]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float lsum = 0.f;
+    mx = warp_max(mx);
+    float lpart = 0.f;
     float acc[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
-    for (int s = 0; s < n_act; ++s) {
-        const float w = fast_exp2(pm[s] - mx);
-        lsum += w * pl[s];
-        const float* src = po + size_t(s) * D;
-        if constexpr (kPer == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
+    for (int base = 0; base < n_act; base += 32) {
+        const int cnt = min(32, n_act - base);
+        float w = 0.f;
+        if (lane < cnt) {
+            w = fast_exp2(pm[base + lane] - mx);
+            lpart += w * pl[base + lane];
+        }
+        for (int j = 0; j < cnt; j += 8) {
+            VecT v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (j + u < cnt) v[u] = *reinterpret_cast<const VecT*>(po + size_t(base + j + u) * D);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float ww = __shfl_sync(0xffffffffu, w, (j + u) & 31);
+                if (j + u < cnt) {
+                    const float* f = reinterpret_cast<const float*>(&v[u]);
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e) acc[e] += ww * f[e];
+                }
+            }
         }
     }
+    const float lsum = warp_sum(lpart);
     const float inv = 1.f / lsum;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j] * inv));
+    for (int j = 0; j < kPer; ++j) out[j] = to_bf16_bits(acc[j] * inv);
     if (lane == 0 && out_lse) *out_lse = (mx + __log2f(lsum)) * kLn2;
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(kTraceCombineBase + blockIdx.x, 2);
 }
 
 // ------------------------------------------------------------------ host side
 
-constexpr int kTileT = 32, kStages = 3, kWarps = 4;
+#ifndef GQA_DEC_TILE_T
+#define GQA_DEC_TILE_T 32
+#endif
+#ifndef GQA_DEC_STAGES
+#define GQA_DEC_STAGES 3
+#endif
+#ifndef GQA_DEC_WARPS
+#define GQA_DEC_WARPS 2
+#endif
+constexpr int kTileT = GQA_DEC_TILE_T, kStages = GQA_DEC_STAGES, kWarps = GQA_DEC_WARPS;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Cluster size for a split count: the largest of 16, 8, 4, 2 dividing it, else 1.
+int cluster_size_for(int ns) {
+    for (int cs : {16, 8, 4, 2})
+        if (ns % cs == 0) return cs;
+    return 1;
+}
 
 struct WsLayout {
     size_t o_off, m_off, l_off, total;
@@ -415,8 +614,9 @@ struct WsLayout {
 
 WsLayout ws_layout(int B, int H_q, int d, int ns) {
     WsLayout w{};
-    if (ns <= 1) return w;
-    const size_t rows = size_t(B) * H_q * ns;
+    const int groups = ns / cluster_size_for(ns);
+    if (groups <= 1) return w;
+    const size_t rows = size_t(B) * H_q * groups;
     w.o_off = 0;
     w.m_off = align256(rows * d * sizeof(float));
     w.l_off = w.m_off + align256(rows * sizeof(float));
@@ -424,25 +624,67 @@ WsLayout ws_layout(int B, int H_q, int d, int ns) {
     return w;
 }
 
-template <int D>
-int launch(const SplitParams& sp, const CUtensorMap& tk, const CUtensorMap& tv,
-           cudaStream_t stream) {
+template <int D, int CS>
+int launch_split(const SplitParams& sp, const CUtensorMap& tk, const CUtensorMap& tv,
+                 cudaStream_t stream) {
     using C = SplitCfg<D, kTileT, kStages, kWarps>;
-    auto kern = split_kernel<D, kTileT, kStages, kWarps>;
+    auto kern = split_kernel<D, kTileT, kStages, kWarps, CS>;
     static bool attr_set = false;  // benign race: setting it twice is harmless
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess)
+                                 C::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+                cudaSuccess)
+            return GQA_ERR_CUDA;
+        if (CS > 8 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess)
             return GQA_ERR_CUDA;
         attr_set = true;
     }
-    dim3 grid(sp.ns, sp.H_kv, sp.B);
-    kern<<<grid, kWarps * 32, C::kSmemBytes, stream>>>(tk, tv, sp);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    if (sp.ns == 1) return GQA_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sp.ns, sp.H_kv, sp.B);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    // Programmatic dependent launch: this grid may start while the previous
+    // kernel in the stream finishes; it reads no global memory before
+    // griddepcontrol.wait.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CS > 1 ? 2 : 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, sp) != cudaSuccess) return GQA_ERR_CUDA;
+    return GQA_OK;
+}
 
+template <int D>
+int launch(const SplitParams& sp, int cs, const CUtensorMap& tk, const CUtensorMap& tv,
+           cudaStream_t stream) {
+    int rc;
+    switch (cs) {
+        case 16: rc = launch_split<D, 16>(sp, tk, tv, stream); break;
+        case 8: rc = launch_split<D, 8>(sp, tk, tv, stream); break;
+        case 4: rc = launch_split<D, 4>(sp, tk, tv, stream); break;
+        case 2: rc = launch_split<D, 2>(sp, tk, tv, stream); break;
+        default: rc = launch_split<D, 1>(sp, tk, tv, stream); break;
+    }
+    if (rc != GQA_OK || sp.n_groups == 1) return rc;
+
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 100) != cudaSuccess)
+            return GQA_ERR_CUDA;
+        attr_set = true;
+    }
     CombineParams cp{sp.part_o, sp.part_m, sp.part_l, sp.seqlens, sp.o, sp.lse,
-                     sp.B, sp.H_q, sp.S_max, sp.ns, sp.L};
+                     sp.B, sp.H_q, sp.S_max, sp.n_groups, int64_t(cs) * sp.L};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((sp.B * sp.H_q + kCombineWarps - 1) / kCombineWarps);
     cfg.blockDim = dim3(kCombineWarps * 32);
@@ -478,8 +720,9 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
         int ns, void* ws, size_t ws_bytes, cudaStream_t stream) {
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
+    const int cs = cluster_size_for(ns);
     const WsLayout wl = ws_layout(B, H_q, d, ns);
-    if (ns > 1) {
+    if (wl.total > 0) {
         if (!ws || ws_bytes < wl.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
             return GQA_ERR_WORKSPACE;
     }
@@ -496,9 +739,10 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.o = o;
     sp.lse = lse;
     uint8_t* w8 = static_cast<uint8_t*>(ws);
-    sp.part_o = ns > 1 ? reinterpret_cast<float*>(w8 + wl.o_off) : nullptr;
-    sp.part_m = ns > 1 ? reinterpret_cast<float*>(w8 + wl.m_off) : nullptr;
-    sp.part_l = ns > 1 ? reinterpret_cast<float*>(w8 + wl.l_off) : nullptr;
+    const bool parts = wl.total > 0;
+    sp.part_o = parts ? reinterpret_cast<float*>(w8 + wl.o_off) : nullptr;
+    sp.part_m = parts ? reinterpret_cast<float*>(w8 + wl.m_off) : nullptr;
+    sp.part_l = parts ? reinterpret_cast<float*>(w8 + wl.l_off) : nullptr;
     sp.status = status;
     sp.B = B;
     sp.H_q = H_q;
@@ -507,8 +751,9 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.S_max = S_max;
     sp.ns = ns;
     sp.L = split_len(S_max, ns);
+    sp.n_groups = ns / cs;
     sp.scale_log2 = scale * kLog2e;
-    return d == 128 ? launch<128>(sp, tk, tv, stream) : launch<64>(sp, tk, tv, stream);
+    return d == 128 ? launch<128>(sp, cs, tk, tv, stream) : launch<64>(sp, cs, tk, tv, stream);
 }
 
 }  // namespace decode
@@ -557,3 +802,17 @@ extern "C" int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint1
     return decode::run(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, ns, ws, bytes,
                        stream);
 }
+
+#ifdef GQA_TRACE
+extern "C" int gqa_attn_trace_dump(void* host, size_t bytes, int clear) {
+    if (bytes > sizeof(gqa::g_trace)) bytes = sizeof(gqa::g_trace);
+    if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(host, gqa::g_trace, bytes) != cudaSuccess) return GQA_ERR_CUDA;
+    if (clear) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, gqa::g_trace) != cudaSuccess) return GQA_ERR_CUDA;
+        if (cudaMemset(p, 0, sizeof(gqa::g_trace)) != cudaSuccess) return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+#endif

@@ -19,6 +19,7 @@ namespace {
 constexpr int kMinKeysPerSplit = 256;   // below this a split is mostly ramp-up
 constexpr int kMaxKeysPerSplit = 1024;  // long rows spread over many blocks
 constexpr int kMaxSplits = 8192;
+constexpr int kClusterSplits = 16;      // splits merged on chip by one thread-block cluster
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -27,8 +28,18 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 extern "C" int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms) {
     if (B <= 0 || H_kv <= 0 || S_max <= 0 || num_sms <= 0) return GQA_ERR_INVALID_ARG;
     const int64_t pairs = int64_t(B) * H_kv;
-    int64_t ns = ceil_div(num_sms, pairs);                     // fill every SM at low batch
+    // Enough blocks to cover the SMs at low batch, in whole clusters of
+    // kClusterSplits splits once a row gets that many (the decode kernel
+    // merges one cluster's splits on chip).
+    int64_t ns = ceil_div(num_sms, pairs);
+    if (ns > kClusterSplits) {
+        const int64_t whole = kClusterSplits * (ns / kClusterSplits);
+        if (5 * pairs * whole >= 4 * int64_t(num_sms)) ns = whole;  // keeps >= 80% of the SMs
+    }
+    // Long rows spread over many blocks.
     ns = std::max<int64_t>(ns, ceil_div(S_max, kMaxKeysPerSplit));
+    if (ns > kClusterSplits) ns = kClusterSplits * ceil_div(ns, kClusterSplits);
+    // But no split shorter than kMinKeysPerSplit keys.
     ns = std::min<int64_t>(ns, std::max(1, S_max / kMinKeysPerSplit));
     ns = std::max<int64_t>(1, std::min<int64_t>(ns, kMaxSplits));
     return int(ns);

@@ -129,9 +129,12 @@ int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * independent derivations bit for bit. Host-only; no GPU needed.
  */
 
-/* Split count for a decode problem: enough (B * H_kv * num_splits) blocks to
- * fill num_sms SMs, with at least 256 keys per split. Returns >= 1, or
- * GQA_ERR_INVALID_ARG. */
+/* Split count for a decode problem: n = ceil(num_sms / (B * H_kv)) blocks per
+ * row (when above 16, rounded down to a multiple of 16 if the blocks then
+ * still cover >= 80% of the SMs), at least
+ * ceil(S_max / 1024) (rounded up to a multiple of 16 when above 16), and at
+ * most max(1, S_max / 256) so no split is shorter than 256 keys. Returns
+ * >= 1, or GQA_ERR_INVALID_ARG. */
 int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
 
 /* Fills starts[s], ends[s] (s < num_splits) with the decode split plan above

@@ -85,15 +85,31 @@ def test_prefill_tile_counts_bit_exact_vs_oracle(L, T_q, S_kv, off, causal):
         assert fut == int((cls == orc.TILE_ALL_FUTURE).sum())
 
 
-def test_pick_num_splits_properties(L):
-    # cfg-shaped cases and a sweep: 1 <= ns <= max(1, S/256); fills the SMs when it can.
-    assert api.gqa_attn_pick_num_splits(1, 8, 8192, 152) == 19
-    for B, H_kv, S, sms in itertools.product((1, 2, 4, 64), (1, 8), (1, 255, 256, 8192, 131072),
+def _pick_reference(B, H_kv, S, sms):
+    # The rule stated in include/gqa_attn.h, restated independently.
+    cdiv = lambda a, b: -(-a // b)
+    n = cdiv(sms, B * H_kv)
+    if n > 16 and B * H_kv * 16 * (n // 16) >= 0.8 * sms:
+        n = 16 * (n // 16)
+    n = max(n, cdiv(S, 1024))
+    if n > 16:
+        n = 16 * cdiv(n, 16)
+    return max(1, min(n, max(1, S // 256), 8192))
+
+
+def test_pick_num_splits_bit_exact_and_properties(L):
+    assert api.gqa_attn_pick_num_splits(1, 8, 8192, 152) == 16       # 8K decode: 8 clusters
+    assert api.gqa_attn_pick_num_splits(4, 8, 131072, 152) == 128    # 128K ragged decode
+    assert api.gqa_attn_pick_num_splits(1, 1, 256, 152) == 1         # tiny decode
+    for B, H_kv, S, sms in itertools.product((1, 2, 3, 4, 64), (1, 2, 8),
+                                             (1, 255, 256, 1000, 8192, 100000, 131072),
                                              (1, 148, 152)):
         ns = api.gqa_attn_pick_num_splits(B, H_kv, S, sms)
+        assert ns == _pick_reference(B, H_kv, S, sms), (B, H_kv, S, sms)
         assert 1 <= ns <= max(1, S // 256)
+        # the blocks cover at least 80% of the SMs whenever the length allows
         if S // 256 >= -(-sms // (B * H_kv)):
-            assert B * H_kv * ns >= sms
+            assert B * H_kv * ns >= 0.8 * sms
     assert api.gqa_attn_pick_num_splits(0, 8, 8192, 152) == api.GQA_ERR_INVALID_ARG
 
 

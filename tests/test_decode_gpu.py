@@ -76,6 +76,18 @@ def test_small_shapes_group_sizes(d, G):
         assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"d={d} G={G} ns={ns}")
 
 
+@pytest.mark.parametrize("d,G", [(128, 8), (64, 4), (128, 1)])
+def test_cluster_merge_every_cluster_size(d, G):
+    # ns = 2, 4, 8, 16 merge one cluster per row on chip; 32, 48, 64 add the
+    # cross-cluster combine; 6 and 24 use clusters of 2 and 8.
+    q, k, v, _ = wl.small_decode(3, 2 * G, 2, d, 3000, seed=700 + d + G)
+    sl = torch.tensor([3000, 1601, 17], dtype=torch.int32)
+    O, L = oracle_decode(q, k, v, sl, 1 / math.sqrt(d))
+    for ns in (2, 4, 6, 8, 16, 24, 32, 48, 64):
+        o, lse = run_decode(q, k, v, sl, ns)
+        assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"d={d} G={G} ns={ns}")
+
+
 @pytest.mark.parametrize("S_max", [1, 15, 16, 17, 31, 32, 33, 100, 255, 1000])
 def test_ragged_and_tiny_lengths(S_max):
     lens = sorted({0, 1, S_max // 2, max(S_max - 1, 0), S_max})
