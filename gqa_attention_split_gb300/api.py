@@ -37,6 +37,7 @@ _SIGNATURES = {
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _S,
                                 _P]),
     "gqa_attn_decode_workspace_size": (_S, [_I, _I, _I, _I]),
+    "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_prefill_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_pick_num_splits": (_I, [_I, _I, _I, _I]),
@@ -97,6 +98,15 @@ def gqa_attn_decode_ws(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, 
                        workspace, workspace_bytes, stream):
     return lib().gqa_attn_decode_ws(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale,
                                     num_splits, workspace, workspace_bytes, stream)
+
+
+def gqa_attn_decode_noalloc(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale,
+                            num_splits, stream):
+    return lib().gqa_attn_decode_noalloc(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max,
+                                         scale, num_splits, stream)
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20  # GQA_NOALLOC_SCRATCH_BYTES
 
 
 def gqa_attn_decode_workspace_size(B, H_q, d, num_splits):

@@ -816,3 +816,117 @@ extern "C" int gqa_attn_trace_dump(void* host, size_t bytes, int clear) {
     return GQA_OK;
 }
 #endif
+
+// ---------------------------------------------------------------------------
+// Decode that allocates no device memory.
+//
+// Some callers cannot call cudaMalloc: a serving process that partitions HBM
+// once at start-up and forbids later allocations, a host that routes every
+// device byte through its own allocator, or a latency-critical path that
+// cannot afford cudaMalloc's implicit device synchronisation. For them the
+// split-KV decode above runs with its scratch (the per-cluster partials and a
+// status word) in fixed arrays that live in this library's module: every GPU
+// that loads the library holds them until the process exits.
+
+#include <mutex>
+
+namespace gqa {
+namespace decode {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ unsigned g_noalloc_status;
+
+struct NoAllocDevice {
+    bool ready;
+    void* scratch;     // device address of g_noalloc_scratch on this device
+    unsigned* status;  // device address of g_noalloc_status on this device
+};
+constexpr int kNoAllocMaxDevices = 64;
+static NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];  // zero-initialised, no heap
+static std::mutex g_noalloc_mu;
+
+// Looks up the device addresses of the two arrays once per device (with that
+// device current). In host code the array names are host-side stand-ins, not
+// device addresses, so they must never be passed to a kernel directly.
+static int noalloc_setup(void** scratch, unsigned** status) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return GQA_ERR_CUDA;
+    if (dev >= kNoAllocMaxDevices) return GQA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        void* a = nullptr;
+        void* s = nullptr;
+        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess) return GQA_ERR_CUDA;
+        if (cudaGetSymbolAddress(&s, g_noalloc_status) != cudaSuccess) return GQA_ERR_CUDA;
+        d.scratch = a;
+        d.status = static_cast<unsigned*>(s);
+        d.ready = true;
+    }
+    *scratch = d.scratch;
+    *status = d.status;
+    return GQA_OK;
+}
+
+}  // namespace decode
+}  // namespace gqa
+
+extern "C" int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                       uint16_t* o, float* lse, const int32_t* seqlens, int B,
+                                       int H_q, int H_kv, int d, int S_max, float scale,
+                                       int num_splits, cudaStream_t stream) {
+    using namespace gqa::decode;
+    int rc = check_args(q, k, v, o, B, H_q, H_kv, d, S_max, scale, num_splits);
+    if (rc != GQA_OK) return rc;
+    if (B == 0) return GQA_OK;
+    int ns = num_splits;
+    if (ns == 0) {
+        int dev = -1, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GQA_ERR_CUDA;
+        ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
+        if (ns < 1) return GQA_ERR_INVALID_ARG;
+    }
+    if (ws_layout(B, H_q, d, ns).total > kNoAllocScratchBytes) return GQA_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    unsigned* status = nullptr;
+    rc = noalloc_setup(&scratch, &status);
+    if (rc != GQA_OK) return rc;
+    // The status word only ever has bits OR-ed in; start each call from zero.
+    if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return GQA_ERR_CUDA;
+
+    // The same launch sequence as gqa_attn_decode, with the fixed scratch and
+    // status word in place of the library-owned ones.
+    const int cs = cluster_size_for(ns);
+    const WsLayout wl = ws_layout(B, H_q, d, ns);
+    CUtensorMap tk, tv;
+    const uint64_t outer = uint64_t(B) * H_kv;
+    if (gqa::encode_tmap_3d_bf16(&tk, k, d, S_max, outer, 64, kTileT,
+                                 CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+        gqa::encode_tmap_3d_bf16(&tv, v, d, S_max, outer, 64, kTileT,
+                                 CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    SplitParams sp{};
+    sp.q = q;
+    sp.seqlens = seqlens;
+    sp.o = o;
+    sp.lse = lse;
+    uint8_t* w8 = static_cast<uint8_t*>(scratch);
+    const bool parts = wl.total > 0;
+    sp.part_o = parts ? reinterpret_cast<float*>(w8 + wl.o_off) : nullptr;
+    sp.part_m = parts ? reinterpret_cast<float*>(w8 + wl.m_off) : nullptr;
+    sp.part_l = parts ? reinterpret_cast<float*>(w8 + wl.l_off) : nullptr;
+    sp.status = status;
+    sp.B = B;
+    sp.H_q = H_q;
+    sp.H_kv = H_kv;
+    sp.G = H_q / H_kv;
+    sp.S_max = S_max;
+    sp.ns = ns;
+    sp.L = gqa::split_len(S_max, ns);
+    sp.n_groups = ns / cs;
+    sp.scale_log2 = scale * kLog2e;
+    return d == 128 ? launch<128>(sp, cs, tk, tv, stream) : launch<64>(sp, cs, tk, tv, stream);
+}

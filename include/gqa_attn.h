@@ -105,6 +105,36 @@ int gqa_attn_decode_ws(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * writes O directly). Returns 0 on invalid sizes as well. */
 size_t gqa_attn_decode_workspace_size(int B, int H_q, int d, int num_splits);
 
+/* gqa_attn_decode for callers that must not allocate device memory. (The page
+ * has no counterpart: this is a deployment option, not part of the method.)
+ * Some callers cannot call cudaMalloc: a serving process that partitions HBM
+ * once at start-up and forbids later allocations, a host that routes every
+ * device byte through its own allocator, or a latency-critical path that
+ * cannot afford cudaMalloc's implicit device synchronisation. This entry
+ * point allocates nothing: the caller passes inputs and outputs exactly as for
+ * gqa_attn_decode, and the scratch the split merge needs lives in a fixed
+ * 8 MiB array inside the library (GQA_NOALLOC_SCRATCH_BYTES), which every GPU
+ * that loads the library holds until the process exits.
+ *   - Returns GQA_ERR_WORKSPACE, without launching, when the problem needs more
+ *     scratch than that: gqa_attn_decode_workspace_size(B, H_q, d, n) must be
+ *     <= GQA_NOALLOC_SCRATCH_BYTES for the split count n in use (the resolved
+ *     one when num_splits == 0).
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array, and it keeps the last call's contents
+ *     (nothing in it needs to start at zero: each call writes every partial
+ *     before reading it). Calls that overlap on the GPU, on any streams, race
+ *     on it: serialise them.
+ *   - Device-detected errors (a clamped seqlen, a bounded wait that ran out)
+ *     go to a status word in the same fixed area; gqa_attn_check() does not
+ *     report them.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            uint16_t* o, float* lse, const int32_t* seqlens,
+                            int B, int H_q, int H_kv, int d, int S_max,
+                            float scale, int num_splits, cudaStream_t stream);
+
 /* --------------------------------------------------------------- prefill --
  * gqa_attn_prefill: T_q new queries at global positions q_offset + t against
  * S_kv keys (the cache already holds the new keys: q_offset + T_q <= S_kv).
