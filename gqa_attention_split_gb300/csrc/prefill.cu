@@ -75,11 +75,6 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// Sum of the two bf16 values packed in x (widening bf16 to fp32 is exact).
-__device__ __forceinline__ float bf16x2_sum(uint32_t x) {
-    return __uint_as_float(x << 16) + __uint_as_float(x & 0xFFFF0000u);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
@@ -234,38 +229,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kSFree + (j & 1)));  // S buffer may be rewritten
 
-            // scale into log2 units, mask the boundary tile, row max
+            // mask the boundary tile (raw scores), row max as a shallow tree
             const int ks = j * BN, ke = min(ks + BN, p.S_kv);
             const bool masked =
                 (p.causal && tile_class(qs, qe, ks, ke) == kTilePartial) || (ke - ks < BN);
-            float mx = -INFINITY;
             if (masked) {
-                const int lim = p.causal ? min(qg, p.S_kv - 1) : p.S_kv - 1;
+                const int lim = (p.causal ? min(qg, p.S_kv - 1) : p.S_kv - 1) - ks;
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    sv[c] = (ks + c <= lim) ? sv[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    sv[c] *= p.scale_log2;
-                    mx = fmaxf(mx, sv[c]);
-                }
+                for (int c = 0; c < BN; ++c) sv[c] = c <= lim ? sv[c] : -INFINITY;
             }
-            const float m_new = fmaxf(m_run, mx);
+            float mx;
+            {
+                float mm[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mm[i] = fmaxf(sv[i], sv[8 + i]);
+#pragma unroll
+                for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mm[i] = fmax3(mm[i], sv[c + i], sv[c + 8 + i]);
+                mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]),
+                           fmaxf(mm[6], mm[7]));
+            }
+            // scale > 0, so the max of the scaled scores is the scaled max
+            const float m_new = fmaxf(m_run, mx * p.scale_log2);
             const bool need = m_new > m_run + kRescaleThreshold;  // true while m_run = -inf
             const float corr = need ? fast_exp2(m_run - m_new) : 1.f;
             const float m_use = need ? m_new : m_run;
-            float rs = 0.f;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                sv[c] = fast_exp2(sv[c] - m_use);
-                rs += sv[c];
-            }
-            l_run = l_run * corr + rs;
-            lb_run *= corr;
             m_run = m_use;
+
+            // p = 2^(s*scale - m) in packed pairs, the row sums of p (fp32) and of
+            // the bf16-rounded p, and P packed to bf16. Four independent pair
+            // accumulators keep the dependency chains short.
+            uint32_t pk[BN / 2];
+            {
+                const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
+                const uint64_t n2 = f2pack(-m_use, -m_use);
+                uint64_t s2[4], b2[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) s2[u] = b2[u] = 0ull;
+#pragma unroll
+                for (int i = 0; i < BN / 2; ++i) {
+                    float x0, x1;
+                    f2unpack(ffma2(f2pack(sv[2 * i], sv[2 * i + 1]), c2, n2), x0, x1);
+                    const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                    s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
+                    pk[i] = pack_bf16x2(e0, e1);
+                    b2[i & 3] = fadd2(b2[i & 3], f2pack(__uint_as_float(pk[i] << 16),
+                                                        __uint_as_float(pk[i] & 0xFFFF0000u)));
+                }
+                float t[8], tb[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
+                    f2unpack(b2[u], tb[2 * u], tb[2 * u + 1]);
+                }
+                const float rs = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+                const float rsb =
+                    ((tb[0] + tb[1]) + (tb[2] + tb[3])) + ((tb[4] + tb[5]) + (tb[6] + tb[7]));
+                l_run = l_run * corr + rs;
+                lb_run = lb_run * corr + rsb;
+            }
 
             // P and O are free once the previous tile's P.V has completed.
             if (j >= 1) {
@@ -274,32 +297,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!alive) break;
                 tc::fence_after_sync();
                 if (__any_sync(0xffffffffu, need)) {
+                    const uint64_t corr2 = f2pack(corr, corr);
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
                         tc::tmem_ld32(lane_base + kTmemO + c * 32, r);
                         tc::tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                        for (int i = 0; i < 16; ++i) {
+                            float a0, a1;
+                            f2unpack(fmul2(f2pack(__uint_as_float(r[2 * i]),
+                                                  __uint_as_float(r[2 * i + 1])),
+                                           corr2),
+                                     a0, a1);
+                            r[2 * i] = __float_as_uint(a0);
+                            r[2 * i + 1] = __float_as_uint(a1);
+                        }
                         tc::tmem_st32(lane_base + kTmemO + c * 32, r);
                     }
                     tc::tmem_wait_st();
                 }
             }
-            // P row -> shared memory, bf16, in the 128-byte swizzled K-major layout
-            float rsb = 0.f;
+            // P row -> shared memory in the 128-byte swizzled K-major layout
 #pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16) {
-                uint4 v;
-                v.x = pack_bf16x2(sv[c16 * 8 + 0], sv[c16 * 8 + 1]);
-                v.y = pack_bf16x2(sv[c16 * 8 + 2], sv[c16 * 8 + 3]);
-                v.z = pack_bf16x2(sv[c16 * 8 + 4], sv[c16 * 8 + 5]);
-                v.w = pack_bf16x2(sv[c16 * 8 + 6], sv[c16 * 8 + 7]);
-                rsb += bf16x2_sum(v.x) + bf16x2_sum(v.y) + bf16x2_sum(v.z) + bf16x2_sum(v.w);
-                *reinterpret_cast<uint4*>(psm + (c16 >> 3) * kBoxBytes + swz128(row, c16 & 7)) = v;
-            }
-            lb_run += rsb;
+            for (int c16 = 0; c16 < BN / 8; ++c16)
+                *reinterpret_cast<uint4*>(psm + (c16 >> 3) * kBoxBytes + swz128(row, c16 & 7)) =
+                    make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
             fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async proxy
             tc::fence_before_sync();
             __syncwarp();
@@ -318,6 +341,346 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
                 tc::tmem_ld32(lane_base + kTmemO + c * 32, r);
+                tc::tmem_wait_ld();
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + c * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv,
+                                          __uint_as_float(r[v4 * 8 + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv,
+                                          __uint_as_float(r[v4 * 8 + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv,
+                                          __uint_as_float(r[v4 * 8 + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv,
+                                          __uint_as_float(r[v4 * 8 + 7]) * inv);
+                        dst[v4] = w;
+                    }
+                }
+            }
+            if (valid && p.lse) p.lse[orow] = (m_run + __log2f(l_run)) * kLn2;
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Two query heads of one KV group per CTA (used when G is even). The page's
+// GQA lever (§5.2, fold the G heads into the matmul M dimension) applied to
+// prefill: every K/V tile loaded into shared memory serves 2 x 128 query
+// rows. P stays in tensor memory (written over its own S columns) and feeds
+// the P.V MMA as the A operand, so shared memory only carries Q, K and V.
+//   warpgroup 0 (72 registers/thread): warp 0 TMA (Q of both heads once,
+//               then K_j, V_j through a 4-slot ring); warp 1 tensor-memory
+//               owner and MMA issuer, order per KV tile j: PV_A(j), S_A(j+1),
+//               PV_B(j), S_B(j+1) (S_A(0), S_B(0) first). An S MMA overwrites
+//               the P the previous PV read; tcgen05.mma operations of one
+//               thread execute in issue order. Warps 2-3 only wait.
+//   warpgroups 1 and 2 (216 registers/thread): softmax of head A and of
+//               head B; while one group computes, the tensor core runs the
+//               other group's MMAs.
+// Register split: 128 x 72 + 256 x 216 = 64512 = 384 threads x 168 at launch.
+
+constexpr int kPairThreads = 384;
+constexpr int kRingSlots = 4;
+constexpr uint32_t kPairQOff = 0;                                // Q_A, then Q_B
+constexpr uint32_t kPairRingOff = 2 * kTileBytes;                // 4 x 32 KB slots
+constexpr uint32_t kPairBarOff = kPairRingOff + kRingSlots * kTileBytes;
+constexpr int kPairSmemBytes = 1024 + kPairBarOff + 256;
+// tensor memory columns
+// S_g (and P_g over its first 64 columns) at g*128; O_g at 256 + g*128.
+__device__ __forceinline__ uint32_t col_s_of(int g) { return uint32_t(g) * 128u; }
+__device__ __forceinline__ uint32_t col_o_of(int g) { return 256u + uint32_t(g) * 128u; }
+
+enum PairBar { pQFull = 0, pSlotFull = 1, pSlotEmpty = 5, pSFull = 9, pPFull = 11, pODone = 13,
+               pDrain = 15, pNumBars = 16 };
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                        const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPairBarOff + pNumBars * 8);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- work item: (batch, KV head, head pair, query block), heaviest first
+    const int pairs = p.H_q / 2;
+    const int bp_count = p.B * pairs;
+    const int mb = p.n_mblocks - 1 - int(blockIdx.x) / bp_count;
+    const int bp = int(blockIdx.x) % bp_count;
+    const int b = bp / pairs, h0 = (bp % pairs) * 2, kvh = h0 / p.G;
+    const int m0 = mb * BM;
+    const int qs = p.q_offset + m0;
+    const int qe = p.q_offset + min(m0 + BM, p.T_q);
+    int n_tiles = (p.S_kv + BN - 1) / BN;
+    if (p.causal) n_tiles = min(n_tiles, (qe - 1) / BN + 1);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(pQFull), 1);
+        for (int s = 0; s < kRingSlots; ++s) {
+            mbar_init(bar(pSlotFull + s), 1);
+            mbar_init(bar(pSlotEmpty + s), 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(bar(pSFull + g), 1);
+            mbar_init(bar(pPFull + g), 4);
+            mbar_init(bar(pODone + g), 1);
+        }
+        mbar_init(bar(pDrain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int n_items = 2 * n_tiles;  // ring items: K_0, V_0, K_1, V_1, ...
+    const int wg = warp >> 2;
+
+    if (wg == 0) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+      if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+            mbar_arrive_expect_tx(bar(pQFull), 2 * kTileBytes);
+            for (int g = 0; g < 2; ++g)
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load(smem_u32(smem + kPairQOff + g * kTileBytes) + hh * kBoxBytes, &tmap_q,
+                             hh * 64, m0, b * p.H_q + h0 + g, bar(pQFull));
+            bool alive = true;
+            int issued = 0;
+            for (int i = 0; i < n_items && alive; ++i) {
+                const int s = i % kRingSlots;
+                if (i >= kRingSlots)
+                    alive = mbar_wait_bounded(bar(pSlotEmpty + s), ((i / kRingSlots) - 1) & 1,
+                                              p.status);
+                if (!alive) break;
+                const CUtensorMap* map = (i & 1) ? &tmap_v : &tmap_k;
+                const uint32_t dst = smem_u32(smem + kPairRingOff + s * kTileBytes);
+                mbar_arrive_expect_tx(bar(pSlotFull + s), kTileBytes);
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load(dst + hh * kBoxBytes, map, hh * 64, (i >> 1) * BN, b * p.H_kv + kvh,
+                             bar(pSlotFull + s));
+                issued = i + 1;
+            }
+            mbar_wait_bounded(bar(pQFull), 0, p.status);
+            for (int i = max(0, issued - kRingSlots); i < issued; ++i)
+                mbar_wait_bounded(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1,
+                                  p.status);
+        }
+      } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false);
+            const uint32_t idesc_pv = tc::idesc_bf16_f32(BM, D, true);
+            auto slot_addr = [&](int i) {
+                return smem_u32(smem + kPairRingOff + (i % kRingSlots) * kTileBytes);
+            };
+            auto wait_item = [&](int i) {
+                return mbar_wait_bounded(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1,
+                                         p.status);
+            };
+            auto issue_s = [&](int g, int j) {  // S_g = Q_g K_j^T
+                const uint32_t qsm = smem_u32(smem + kPairQOff + g * kTileBytes);
+                const uint32_t ksm = slot_addr(2 * j);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    tc::mma_ss(tmem + col_s_of(g), tc::sdesc_sw128(qsm + off, 16, 1024),
+                               tc::sdesc_sw128(ksm + off, 16, 1024), idesc_s, kk > 0);
+                }
+                tc::commit(bar(pSFull + g));
+            };
+            auto issue_pv = [&](int g, int j) {  // O_g += P_g V_j, P_g from tensor memory
+                const uint32_t vsm = slot_addr(2 * j + 1);
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    mma_ts(tmem + col_o_of(g), tmem + col_s_of(g) + ks * 8,
+                           tc::sdesc_sw128(vsm + ks * 2048, kBoxBytes, 1024), idesc_pv,
+                           (j > 0 || ks > 0) ? 1u : 0u);
+            };
+            bool alive = mbar_wait_bounded(bar(pQFull), 0, p.status) && wait_item(0);
+            if (alive) {
+                tc::fence_after_sync();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc::commit(bar(pSlotEmpty + 0));  // K_0 read by both S MMAs
+            }
+            for (int j = 0; j < n_tiles && alive; ++j) {
+                const bool more = j + 1 < n_tiles;
+                for (int g = 0; g < 2 && alive; ++g) {
+                    alive = mbar_wait_bounded(bar(pPFull + g), j & 1, p.status);
+                    if (alive && g == 0) alive = wait_item(2 * j + 1);  // V_j
+                    if (alive && g == 0 && more) alive = wait_item(2 * j + 2);  // K_{j+1}
+                    if (!alive) break;
+                    tc::fence_after_sync();
+                    issue_pv(g, j);
+                    if (g == 1) tc::commit(bar(pSlotEmpty + (2 * j + 1) % kRingSlots));  // V_j
+                    if (more) {
+                        issue_s(g, j + 1);
+                        if (g == 1)
+                            tc::commit(bar(pSlotEmpty + (2 * j + 2) % kRingSlots));  // K_{j+1}
+                    } else {
+                        tc::commit(bar(pODone + g));
+                    }
+                }
+            }
+            tc::commit(bar(pDrain));
+            mbar_wait_bounded(bar(pDrain), 0, p.status);
+        }
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+        // ------------------------------------------------ softmax warpgroups
+        const int g = wg - 1;                 // 0: head h0, 1: head h0 + 1
+        const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31
+        const int row = quad * 32 + lane;
+        const int qg = qs + row;
+        const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
+        const uint32_t col_s = col_s_of(g), col_o = col_o_of(g);
+        float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
+        bool alive = true;
+        for (int j = 0; j < n_tiles && alive; ++j) {
+            alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pSFull + g), j & 1, p.status));
+            if (!alive) break;
+            tc::fence_after_sync();
+            float sv[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tc::tmem_ld32(lane_base + col_s + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[i]);
+            }
+            tc::tmem_wait_ld();
+
+            const int ks = j * BN, ke = min(ks + BN, p.S_kv);
+            const bool masked =
+                (p.causal && tile_class(qs, qe, ks, ke) == kTilePartial) || (ke - ks < BN);
+            if (masked) {
+                const int lim = (p.causal ? min(qg, p.S_kv - 1) : p.S_kv - 1) - ks;
+#pragma unroll
+                for (int c = 0; c < BN; ++c) sv[c] = c <= lim ? sv[c] : -INFINITY;
+            }
+            float mx;
+            {
+                float mm[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mm[i] = fmaxf(sv[i], sv[8 + i]);
+#pragma unroll
+                for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mm[i] = fmax3(mm[i], sv[c + i], sv[c + 8 + i]);
+                mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]),
+                           fmaxf(mm[6], mm[7]));
+            }
+            const float m_new = fmaxf(m_run, mx * p.scale_log2);
+            const bool need = m_new > m_run + kRescaleThreshold;
+            const float corr = need ? fast_exp2(m_run - m_new) : 1.f;
+            const float m_use = need ? m_new : m_run;
+            m_run = m_use;
+            // O is complete here: this tile's S MMA was issued after the
+            // previous P.V, and tcgen05 MMAs complete in order.
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                const uint64_t corr2 = f2pack(corr, corr);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(lane_base + col_o + c * 32, r);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float a0, a1;
+                        f2unpack(fmul2(f2pack(__uint_as_float(r[2 * i]),
+                                              __uint_as_float(r[2 * i + 1])),
+                                       corr2),
+                                 a0, a1);
+                        r[2 * i] = __float_as_uint(a0);
+                        r[2 * i + 1] = __float_as_uint(a1);
+                    }
+                    tc::tmem_st32(lane_base + col_o + c * 32, r);
+                }
+            }
+            // p = 2^(s*scale - m): sums of p and of bf16(p); P (bf16 pairs,
+            // lower key in the low half) over the first 64 columns of S.
+            const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
+            const uint64_t n2 = f2pack(-m_use, -m_use);
+            uint64_t s2[4], b2[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s2[u] = b2[u] = 0ull;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = half * 64 + 2 * i;
+                    float x0, x1;
+                    f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), c2, n2), x0, x1);
+                    const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                    s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
+                    pk[i] = pack_bf16x2(e0, e1);
+                    b2[i & 3] = fadd2(b2[i & 3], f2pack(__uint_as_float(pk[i] << 16),
+                                                        __uint_as_float(pk[i] & 0xFFFF0000u)));
+                }
+                tc::tmem_st32(lane_base + col_s + half * 32, pk);
+            }
+            {
+                float t[8], tb[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
+                    f2unpack(b2[u], tb[2 * u], tb[2 * u + 1]);
+                }
+                l_run = l_run * corr +
+                        (((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7])));
+                lb_run = lb_run * corr +
+                         (((tb[0] + tb[1]) + (tb[2] + tb[3])) + ((tb[4] + tb[5]) + (tb[6] + tb[7])));
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(pPFull + g));
+        }
+
+        // ---- epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
+        if (alive)
+            alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pODone + g), 0, p.status));
+        if (alive) {
+            tc::fence_after_sync();
+            const bool valid = m0 + row < p.T_q;
+            const float inv = 1.f / lb_run;
+            const size_t orow = (size_t(b) * p.H_q + h0 + g) * p.T_q + m0 + row;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tc::tmem_ld32(lane_base + col_o + c * 32, r);
                 tc::tmem_wait_ld();
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + c * 32);
@@ -404,13 +767,22 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
+                                 kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) != cudaSuccess)
             return GQA_ERR_CUDA;
         attr_set = true;
     }
-    const int64_t items = int64_t(prm.n_mblocks) * B * H_q;
+    // Even group sizes run two heads of a KV group per CTA; odd ones one head.
+    const bool pair = prm.G % 2 == 0;
+    const int64_t items = int64_t(prm.n_mblocks) * B * (pair ? H_q / 2 : H_q);
     if (items > 0x7fffffff) return GQA_ERR_UNSUPPORTED;
-    prefill_kernel<<<dim3(unsigned(items)), kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
+    if (pair)
+        prefill_pair_kernel<<<dim3(unsigned(items)), kPairThreads, kPairSmemBytes, stream>>>(
+            tq, tk, tv, prm);
+    else
+        prefill_kernel<<<dim3(unsigned(items)), kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;
 }
