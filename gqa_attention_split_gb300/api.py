@@ -47,6 +47,7 @@ _SIGNATURES = {
     "gqa_attn_prefill_block_m": (_I, []),
     "gqa_attn_prefill_block_n": (_I, []),
     "gqa_attn_check": (_I, [_P]),
+    "gqa_attn_debug_inject_timeout": (_I, [_I]),
     "gqa_attn_strerror": (ctypes.c_char_p, [_I]),
     "gqa_attn_version": (_I, []),
 }
@@ -158,6 +159,10 @@ def gqa_attn_prefill_block_n():
 
 def gqa_attn_check(stream=None):
     return lib().gqa_attn_check(stream)
+
+
+def gqa_attn_debug_inject_timeout(launches):
+    return lib().gqa_attn_debug_inject_timeout(launches)
 
 
 def strerror(code: int) -> str:

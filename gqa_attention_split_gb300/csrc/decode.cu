@@ -24,8 +24,10 @@
 //   into the scores.
 // * Level 2 of the reduction: the warps of a CTA merge in shared memory, then
 //   the CS CTAs of a thread-block cluster (consecutive splits of one KV head)
-//   merge through distributed shared memory, in cluster-rank order. If one
-//   cluster spans the whole row it writes O and lse directly.
+//   store one record per head into the shared memory of that head's owner
+//   CTA (distributed shared memory), a cluster barrier makes the records
+//   visible, and the owner folds them in cluster-rank order. If one cluster
+//   spans the whole row it writes O and lse directly.
 // * Level 1 (only when a row spans several clusters): each cluster writes a
 //   partial to the workspace and a PDL-launched combine kernel merges them in
 //   group order.
@@ -38,6 +40,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "gqa_attn.h"
@@ -64,6 +67,7 @@ struct SplitParams {
     unsigned* status;
     int B, H_q, H_kv, G, S_max, ns, L, n_groups;
     float scale_log2;         // scale * log2(e)
+    int inject_timeout;       // test hook: block (0,0,0) withholds its first copy
 };
 
 template <int D, int TILE_T, int STAGES, int WARPS>
@@ -79,16 +83,14 @@ struct SplitCfg {
     static constexpr int kRec = 4 + D;
     static constexpr int kRecBytes = kRec * 4;
     static constexpr int kWarpMergeFloats = (WARPS - 1) * (D / 16 * 4 + 4) * 32;
-    static constexpr int kSendFloats = kMaxG * kRec;
-    static constexpr int kMergeBytes = (kSendFloats + kWarpMergeFloats) * 4;
+    static constexpr int kMergeBytes = kWarpMergeFloats * 4;
     static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
     // Inbound records: [heads per rank][CS][kRec]. A rank owns ceil(8 / CS)
     // heads, so it receives at most 16 records for any CS <= 16.
     static constexpr int kRecvOffset = kDataBytes;
     static constexpr int kRecvBytes = 2 * kMaxG * kRecBytes;
     static constexpr int kBarOffset = kRecvOffset + kRecvBytes;
-    static constexpr int kSmemBytes =
-        1024 /*alignment slack*/ + kBarOffset + (WARPS * STAGES + 1) * 8;
+    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kBarOffset + WARPS * STAGES * 8;
     static constexpr int kMT = TILE_T / 16;             // 16-key m-tiles per stage
     static constexpr int kKC = D / 16;                  // 16-wide k-chunks of a head dim
     static_assert(TILE_T % 16 == 0 && TILE_T <= 256, "tile");
@@ -175,22 +177,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     uint8_t* ring = smem + size_t(warp) * STAGES * C::kStageBytes;
     // Heads whose cluster merge this CTA owns: h = rank, rank + CS, ... < G.
     const int n_own = CS > 1 && rank < p.G ? (p.G - rank + CS - 1) / CS : 0;
-    uint64_t* recv_bar = reinterpret_cast<uint64_t*>(smem + C::kBarOffset) + WARPS * STAGES;
     float* recv = reinterpret_cast<float*>(smem + C::kRecvOffset);  // [n_own][CS][kRec]
     if (lane == 0) {
         for (int i = 0; i < STAGES; ++i) mbar_init(smem_u32(&bars[i]), 1);
-        if (CS > 1 && warp == 0) {
-            // Armed before any peer can send: the peers' records complete it.
-            mbar_init(smem_u32(recv_bar), 1);
-            if (n_own > 0) mbar_arrive_expect_tx(smem_u32(recv_bar), n_own * CS * C::kRecBytes);
-        }
         fence_mbar_init();
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
     }
     __syncwarp();
-    // Cluster: publish the armed barrier now; wait for the peers' only before
-    // sending to them (by then every CTA has long passed this point).
+    // Cluster barrier, phase 0: every CTA of the cluster is running before any
+    // of them stores into another's shared memory (arrive now, wait later).
     if constexpr (CS > 1) cluster_arrive_release();
 
     pdl_wait_primary();  // everything below may read what earlier kernels wrote
@@ -235,9 +231,13 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
     };
 
+    // Test hook: the first block withholds its first copy, so its first wait
+    // runs out and reports kStatusTimeout (nothing faults, nothing hangs).
+    const bool withhold = p.inject_timeout && s == 0 && kv == 0 && b == 0 && warp == 0;
     int issued = 0;
     if (lane == 0) {
-        for (; issued < STAGES && issued < my_n; ++issued) issue(issued);
+        for (; issued < STAGES && issued < my_n; ++issued)
+            if (!(withhold && issued == 0)) issue(issued);
     }
     issued = __shfl_sync(0xffffffffu, issued, 0);
 
@@ -264,10 +264,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     int waited = 0;
     for (int i = 0; i < my_n; ++i) {
         const int slot = i % STAGES;
-        if (alive) alive = mbar_wait_bounded(smem_u32(&bars[slot]), (i / STAGES) & 1, p.status);
-        alive = __all_sync(0xffffffffu, alive);  // keep the warp's control flow uniform
+        if (alive) {
+            alive = mbar_wait_bounded(smem_u32(&bars[slot]), (i / STAGES) & 1, p.status);
+            alive = __all_sync(0xffffffffu, alive);  // keep the warp's control flow uniform
+            if (alive) waited = i + 1;                // copies observed complete so far
+        }
         if (i == 0 && threadIdx.x == 0) GQA_TRACE_STAMP(blin, 1);
-        waited = i + 1;
         const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
         const int tok0 = r.start + (warp + i * WARPS) * TILE_T;
@@ -353,9 +355,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         if (alive && issued < my_n) ++issued;
     }
     // A wait that ran out may leave copies in flight: wait for them (bounded)
-    // before the shared memory is reused or released.
+    // before the shared memory is reused or released. A withheld copy was
+    // never issued, so there is nothing of it to wait for.
     for (int i = waited; i < issued; ++i)
-        mbar_wait_bounded(smem_u32(&bars[i % STAGES]), (i / STAGES) & 1, p.status);
+        if (!(withhold && i == 0))
+            mbar_wait_bounded(smem_u32(&bars[i % STAGES]), (i / STAGES) & 1, p.status);
 
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // merges them fragment by fragment in registers (warp order fixed).
     constexpr int kFrag = C::kKC * 4 + 4;  // accumulators, then m0, m1, l0, l1
     float* wbuf = reinterpret_cast<float*>(smem);  // [WARPS-1][kFrag][32]
-    float* rec = wbuf + C::kWarpMergeFloats;       // [8][kRec] records to send (clusters)
+    if constexpr (CS > 1) cluster_wait_acquire();  // phase 0 (long complete by now)
     __syncthreads();  // every warp is done with its ring
     if (warp > 0) {
         float* dst = wbuf + (warp - 1) * kFrag * 32 + lane;
@@ -420,7 +424,19 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             }
         }
         // Warp 0 now holds the CTA partial: lane (g, c) has heads 2c, 2c+1 at
-        // dims md*16 + g (+8).
+        // dims md*16 + g (+8). Without a cluster it is the result (or this
+        // split's partial). With one, each head's record {m, l, 0, 0, O[D]}
+        // goes straight from registers into slot [h / CS][rank] of the head's
+        // owner, rank h % CS, as plain distributed-shared-memory stores.
+        uint32_t rbase[2] = {0u, 0u};
+        if constexpr (CS > 1) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = 2 * c + e;
+                rbase[e] = map_to_rank(smem_u32(recv + ((h / CS) * CS + rank) * C::kRec),
+                                       uint32_t(h % CS));
+            }
+        }
 #pragma unroll
         for (int md = 0; md < C::kKC; ++md) {
 #pragma unroll
@@ -428,47 +444,40 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 const int dim = md * 16 + g + (e >> 1) * 8;
                 const int head = 2 * c + (e & 1);
                 const float mm = (e & 1) ? ms1 : ms0, ll = (e & 1) ? l1 : l0;
-                if constexpr (CS == 1) {
-                    if (head < p.G)
+                if (head < p.G) {
+                    if constexpr (CS == 1)
                         emit(p, size_t(b) * p.H_q + kv * p.G + head, gi, dim, D, mm, ll,
                              acc[md][e]);
-                } else {
-                    rec[head * C::kRec + 4 + dim] = acc[md][e];
+                    else
+                        st_dsmem(rbase[e & 1] + (4 + dim) * 4, acc[md][e]);
                 }
             }
         }
         if (CS > 1 && g == 0) {
-            rec[(2 * c) * C::kRec + 0] = ms0;
-            rec[(2 * c) * C::kRec + 1] = l0;
-            rec[(2 * c + 1) * C::kRec + 0] = ms1;
-            rec[(2 * c + 1) * C::kRec + 1] = l1;
+            if (2 * c < p.G) {
+                st_dsmem(rbase[0] + 0, ms0);
+                st_dsmem(rbase[0] + 4, l0);
+            }
+            if (2 * c + 1 < p.G) {
+                st_dsmem(rbase[1] + 0, ms1);
+                st_dsmem(rbase[1] + 4, l1);
+            }
         }
-        if constexpr (CS > 1) fence_proxy_async_smem();  // records -> async proxy
-        __syncwarp();
     }
 
     if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 4);
     if constexpr (CS > 1) {
-        // ---- level 2b: push head h's record to its owner, rank h % CS, which
-        // merges the CS records of each head it owns in rank order.
-        cluster_wait_acquire();  // every peer's receive barrier is armed
+        // ---- level 2b. Cluster barrier, phase 1: each thread's stores are
+        // released by its arrive and acquired by every wait, so all records
+        // are in their owners' shared memory. No CTA touches another's shared
+        // memory after this point, so none can outlive a store aimed at it.
+        cluster_arrive_release();
+        cluster_wait_acquire();
         if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 6);
-        if (warp == 0 && lane < p.G) {
-            const int h = lane, owner = h % CS;
-            const uint32_t src = smem_u32(rec + h * C::kRec);
-            const uint32_t dst = smem_u32(recv + ((h / CS) * CS + rank) * C::kRec);
-            bulk_copy_to_peer(map_to_rank(dst, owner), src, C::kRecBytes,
-                              map_to_rank(smem_u32(recv_bar), owner));
-            bulk_commit();
-        }
-        bool got = true;
-        if (n_own > 0) got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(recv_bar), 0,
-                                                                         p.status));
-        if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 7);
         // Per owned head, warp 0 alone: lane q holds sender q's (m, l), the
         // weights come from two warp reductions, and each lane folds the CS
-        // records over its D/32 dims with vector loads.
-        if (got && warp == 0) {
+        // records over its D/32 dims with vector loads (rank order fixed).
+        if (warp == 0) {
             constexpr int kPer = D / 32;
             using VecT = typename std::conditional<kPer == 4, float4, float2>::type;
             for (int j = 0; j < n_own; ++j) {
@@ -495,8 +504,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 for (int e = 0; e < kPer; ++e) emit(p, row, gi, lane * kPer + e, D, mstar, lsum, o[e]);
             }
         }
-        // Our records must be read out before this CTA's shared memory goes away.
-        if (warp == 0 && lane < p.G) bulk_wait_read_all();
+        if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 7);
     }
     if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 3);
 }
@@ -715,6 +723,9 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
     return GQA_OK;
 }
 
+// Test hook (gqa_attn_debug_inject_timeout): launches left to inject.
+std::atomic<int> g_inject_timeout{0};
+
 int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse,
         const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max, float scale,
         int ns, void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -753,6 +764,11 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.L = split_len(S_max, ns);
     sp.n_groups = ns / cs;
     sp.scale_log2 = scale * kLog2e;
+    for (int n = g_inject_timeout.load(); n > 0; n = g_inject_timeout.load())
+        if (g_inject_timeout.compare_exchange_weak(n, n - 1)) {
+            sp.inject_timeout = 1;
+            break;
+        }
     return d == 128 ? launch<128>(sp, cs, tk, tv, stream) : launch<64>(sp, cs, tk, tv, stream);
 }
 
@@ -760,6 +776,12 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
 }  // namespace gqa
 
 using namespace gqa;
+
+extern "C" int gqa_attn_debug_inject_timeout(int launches) {
+    if (launches < 0) return GQA_ERR_INVALID_ARG;
+    decode::g_inject_timeout.store(launches);
+    return GQA_OK;
+}
 
 extern "C" size_t gqa_attn_decode_workspace_size(int B, int H_q, int d, int num_splits) {
     if (B < 0 || H_q <= 0 || (d != 64 && d != 128) || num_splits <= 0) return 0;

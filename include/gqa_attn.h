@@ -193,6 +193,15 @@ int gqa_attn_prefill_block_n(void);
  * GQA_ERR_DEVICE_BAD_INPUT or GQA_ERR_CUDA. */
 int gqa_attn_check(cudaStream_t stream);
 
+/* Test hook for failure reporting: the next `launches` gqa_attn_decode /
+ * gqa_attn_decode_ws calls each make their first block withhold its first
+ * K/V copy. That block's bounded wait then runs out (after about one second),
+ * the kernel records the timeout in the device status word and finishes
+ * normally, and gqa_attn_check() returns GQA_ERR_DEVICE_TIMEOUT. The output of
+ * such a call is undefined; nothing faults and later calls are unaffected.
+ * 0 disarms. Returns GQA_OK or GQA_ERR_INVALID_ARG (launches < 0). */
+int gqa_attn_debug_inject_timeout(int launches);
+
 /* Static, human-readable text for a return code. */
 const char* gqa_attn_strerror(int code);
 
