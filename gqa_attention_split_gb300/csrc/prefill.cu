@@ -34,6 +34,7 @@
 #include "ptx.cuh"
 #include "runtime.cuh"
 #include "tcgen05.cuh"
+#include "trace.cuh"
 
 namespace gqa {
 namespace prefill {
@@ -372,35 +373,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Two query heads of one KV group per CTA (used when G is even). The page's
-// GQA lever (§5.2, fold the G heads into the matmul M dimension) applied to
-// prefill: every K/V tile loaded into shared memory serves 2 x 128 query
-// rows. P stays in tensor memory (written over its own S columns) and feeds
-// the P.V MMA as the A operand, so shared memory only carries Q, K and V.
-//   warpgroup 0 (72 registers/thread): warp 0 TMA (Q of both heads once,
-//               then K_j, V_j through a 4-slot ring); warp 1 tensor-memory
-//               owner and MMA issuer, order per KV tile j: PV_A(j), S_A(j+1),
-//               PV_B(j), S_B(j+1) (S_A(0), S_B(0) first). An S MMA overwrites
-//               the P the previous PV read; tcgen05.mma operations of one
-//               thread execute in issue order. Warps 2-3 only wait.
-//   warpgroups 1 and 2 (216 registers/thread): softmax of head A and of
-//               head B; while one group computes, the tensor core runs the
-//               other group's MMAs.
-// Register split: 128 x 72 + 256 x 216 = 64512 = 384 threads x 168 at launch.
+// Two query heads of one KV group per work item (used when G is even). The
+// page's GQA lever (§5.2, fold the G heads into the matmul M dimension)
+// applied to prefill: every K/V tile loaded into shared memory serves 2 x 128
+// query rows. P stays in tensor memory (written over its own S columns) and
+// feeds the P.V MMA as the A operand, so shared memory only carries Q, K, V.
+//
+// Persistent: one CTA per SM walks the work items heaviest first (snake order
+// over the CTAs), so the next item's Q load and first S overlap the previous
+// item's epilogue, and the tensor memory is allocated once.
+//   warpgroup 0 (104 registers/thread): warp 0 TMA (per item: Q of both heads,
+//               then K_j, V_j through a 4-slot ring); warp 1 owns the tensor
+//               memory; warps 1 and 2 each issue one head's MMAs, per KV tile
+//               j: PV_g(j) then S_g(j+1). An S MMA overwrites the P its
+//               thread's previous PV read; the tcgen05.mma operations of one
+//               thread execute in issue order. Warp 3 only waits.
+//   warpgroups 1 and 2 (200 registers/thread): softmax of head A and of
+//               head B, then that head's epilogue; while one group computes,
+//               the tensor core runs the other group's MMAs.
+// Register split: 128 x 104 + 256 x 200 = 64512 = 384 threads x 168 at launch.
+// Every barrier phase is counted across items: the k-th completion of a
+// barrier has parity k & 1.
 
 constexpr int kPairThreads = 384;
+// Four 32 KB slots: ring item r (K_j or V_j of some work item) reuses the
+// slot of item r - 4; the loads land well before their MMAs.
 constexpr int kRingSlots = 4;
 constexpr uint32_t kPairQOff = 0;                                // Q_A, then Q_B
-constexpr uint32_t kPairRingOff = 2 * kTileBytes;                // 4 x 32 KB slots
+constexpr uint32_t kPairRingOff = 2 * kTileBytes;                // kRingSlots x 32 KB
 constexpr uint32_t kPairBarOff = kPairRingOff + kRingSlots * kTileBytes;
 constexpr int kPairSmemBytes = 1024 + kPairBarOff + 256;
-// tensor memory columns
+static_assert(kPairSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
+static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
 // S_g (and P_g over its first 64 columns) at g*128; O_g at 256 + g*128.
 __device__ __forceinline__ uint32_t col_s_of(int g) { return uint32_t(g) * 128u; }
 __device__ __forceinline__ uint32_t col_o_of(int g) { return 256u + uint32_t(g) * 128u; }
 
-enum PairBar { pQFull = 0, pSlotFull = 1, pSlotEmpty = 5, pSFull = 9, pPFull = 11, pODone = 13,
-               pDrain = 15, pNumBars = 16 };
+enum PairBar {
+    pQFull = 0,                        // Q of both heads landed (per item)
+    pQEmpty = 1,                       // both issuers are done with Q (count 2)
+    pSlotFull = 2,                     // x kRingSlots
+    pSlotEmpty = pSlotFull + kRingSlots,  // x kRingSlots, released by both issuers
+    pSFull = pSlotEmpty + kRingSlots,  // x2: S_g ready (per tile)
+    pPFull = pSFull + 2,               // x2: P_g ready (4 softmax warps)
+    pODone = pPFull + 2,               // x2: O_g final (per item)
+    pDrain = pODone + 2,               // the MMA issuer's last commit
+    pNumBars = pDrain + 1
+};
+static_assert(pNumBars * 8 + 4 <= 256, "barrier area");
 
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -410,6 +430,30 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// One work item: a 128-row query block of two adjacent query heads of one
+// KV group. Items are numbered heaviest first (query blocks from the last
+// one down), and a CTA takes items c, 2G-1-c, 2G+c, ... (snake order).
+struct PairItem {
+    int b, h0, kvh, m0, qs, qe, n_tiles;
+};
+
+__device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int L = it * G + ((it & 1) ? G - 1 - c : c);
+    const int pairs = p.H_q / 2, bp_count = p.B * pairs;
+    if (L >= p.n_mblocks * bp_count) return false;
+    const int mb = p.n_mblocks - 1 - L / bp_count, bp = L % bp_count;
+    w.b = bp / pairs;
+    w.h0 = (bp % pairs) * 2;
+    w.kvh = w.h0 / p.G;
+    w.m0 = mb * BM;
+    w.qs = p.q_offset + w.m0;
+    w.qe = p.q_offset + min(w.m0 + BM, p.T_q);
+    w.n_tiles = (p.S_kv + BN - 1) / BN;
+    if (p.causal) w.n_tiles = min(w.n_tiles, (w.qe - 1) / BN + 1);  // all-future tiles skipped
+    return true;
 }
 
 __global__ void __launch_bounds__(kPairThreads, 1)
@@ -424,20 +468,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work item: (batch, KV head, head pair, query block), heaviest first
-    const int pairs = p.H_q / 2;
-    const int bp_count = p.B * pairs;
-    const int mb = p.n_mblocks - 1 - int(blockIdx.x) / bp_count;
-    const int bp = int(blockIdx.x) % bp_count;
-    const int b = bp / pairs, h0 = (bp % pairs) * 2, kvh = h0 / p.G;
-    const int m0 = mb * BM;
-    const int qs = p.q_offset + m0;
-    const int qe = p.q_offset + min(m0 + BM, p.T_q);
-    int n_tiles = (p.S_kv + BN - 1) / BN;
-    if (p.causal) n_tiles = min(n_tiles, (qe - 1) / BN + 1);
-
     if (threadIdx.x == 0) {
         mbar_init(bar(pQFull), 1);
+        mbar_init(bar(pQEmpty), 1);
         for (int s = 0; s < kRingSlots; ++s) {
             mbar_init(bar(pSlotFull + s), 1);
             mbar_init(bar(pSlotEmpty + s), 1);
@@ -458,225 +491,255 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int n_items = 2 * n_tiles;  // ring items: K_0, V_0, K_1, V_1, ...
     const int wg = warp >> 2;
+    PairItem w;
 
     if (wg == 0) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
-      if (warp == 0) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
+      if (warp == 0 && lane == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmap_q);
-            tma_prefetch_desc(&tmap_k);
-            tma_prefetch_desc(&tmap_v);
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+        bool alive = true;
+        int r = 0;        // ring items issued so far, over all work items
+        int q_loads = 0;  // Q loads issued (one per work item)
+        for (int it = 0; alive && pair_item(p, it, w); ++it) {
+            // Q of both heads; the previous item's last S MMAs must be done.
+            if (it > 0) alive = mbar_wait_bounded(bar(pQEmpty), (it - 1) & 1, p.status);
+            if (!alive) break;
             mbar_arrive_expect_tx(bar(pQFull), 2 * kTileBytes);
             for (int g = 0; g < 2; ++g)
                 for (int hh = 0; hh < 2; ++hh)
                     tma_load(smem_u32(smem + kPairQOff + g * kTileBytes) + hh * kBoxBytes, &tmap_q,
-                             hh * 64, m0, b * p.H_q + h0 + g, bar(pQFull));
-            bool alive = true;
-            int issued = 0;
-            for (int i = 0; i < n_items && alive; ++i) {
-                const int s = i % kRingSlots;
-                if (i >= kRingSlots)
-                    alive = mbar_wait_bounded(bar(pSlotEmpty + s), ((i / kRingSlots) - 1) & 1,
+                             hh * 64, w.m0, w.b * p.H_q + w.h0 + g, bar(pQFull));
+            q_loads = it + 1;
+            for (int i = 0; i < 2 * w.n_tiles; ++i, ++r) {  // K_0, V_0, K_1, V_1, ...
+                const int s = r % kRingSlots;
+                if (r >= kRingSlots)
+                    alive = mbar_wait_bounded(bar(pSlotEmpty + s), ((r / kRingSlots) - 1) & 1,
                                               p.status);
                 if (!alive) break;
                 const CUtensorMap* map = (i & 1) ? &tmap_v : &tmap_k;
                 const uint32_t dst = smem_u32(smem + kPairRingOff + s * kTileBytes);
                 mbar_arrive_expect_tx(bar(pSlotFull + s), kTileBytes);
                 for (int hh = 0; hh < 2; ++hh)
-                    tma_load(dst + hh * kBoxBytes, map, hh * 64, (i >> 1) * BN, b * p.H_kv + kvh,
-                             bar(pSlotFull + s));
-                issued = i + 1;
+                    tma_load(dst + hh * kBoxBytes, map, hh * 64, (i >> 1) * BN,
+                             w.b * p.H_kv + w.kvh, bar(pSlotFull + s));
             }
-            mbar_wait_bounded(bar(pQFull), 0, p.status);
-            for (int i = max(0, issued - kRingSlots); i < issued; ++i)
-                mbar_wait_bounded(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1,
-                                  p.status);
         }
-      } else if (warp == 1) {
+        // Every copy still in flight lands before the CTA exits (only the
+        // last kRingSlots ring items and the last Q can be outstanding).
+        if (q_loads > 0) mbar_wait_bounded(bar(pQFull), (q_loads - 1) & 1, p.status);
+        for (int i = max(0, r - kRingSlots); i < r; ++i)
+            mbar_wait_bounded(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1, p.status);
+      } else if (warp == 1 && lane == 0) {
         // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false);
-            const uint32_t idesc_pv = tc::idesc_bf16_f32(BM, D, true);
-            auto slot_addr = [&](int i) {
-                return smem_u32(smem + kPairRingOff + (i % kRingSlots) * kTileBytes);
-            };
-            auto wait_item = [&](int i) {
-                return mbar_wait_bounded(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1,
-                                         p.status);
-            };
-            auto issue_s = [&](int g, int j) {  // S_g = Q_g K_j^T
-                const uint32_t qsm = smem_u32(smem + kPairQOff + g * kTileBytes);
-                const uint32_t ksm = slot_addr(2 * j);
+        // Per KV tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1); S_A(0), S_B(0)
+        // of an item follow the previous item's last PV MMAs.
+        const uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false);
+        const uint32_t idesc_pv = tc::idesc_bf16_f32(BM, D, true);
+        auto slot_addr = [&](int i) {
+            return smem_u32(smem + kPairRingOff + (i % kRingSlots) * kTileBytes);
+        };
+        auto wait_item = [&](int i) {
+            return mbar_wait_fast(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1, p.status);
+        };
+        // Descriptors are built once per operand; each k-step adds its byte
+        // offset >> 4 to the 14-bit start-address field (shared addresses
+        // stay below 256 KB, so the field never carries out).
+        const uint64_t qdesc0 = tc::sdesc_sw128(smem_u32(smem + kPairQOff), 16, 1024);
+        const uint64_t qdesc1 = tc::sdesc_sw128(smem_u32(smem + kPairQOff + kTileBytes), 16, 1024);
+        auto issue_s = [&](int g, int ri) {  // S_g = Q_g K^T, K in ring item ri
+            const uint64_t qdesc = g ? qdesc1 : qdesc0;
+            const uint64_t kdesc = tc::sdesc_sw128(slot_addr(ri), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    tc::mma_ss(tmem + col_s_of(g), tc::sdesc_sw128(qsm + off, 16, 1024),
-                               tc::sdesc_sw128(ksm + off, 16, 1024), idesc_s, kk > 0);
-                }
-                tc::commit(bar(pSFull + g));
-            };
-            auto issue_pv = [&](int g, int j) {  // O_g += P_g V_j, P_g from tensor memory
-                const uint32_t vsm = slot_addr(2 * j + 1);
-#pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks)
-                    mma_ts(tmem + col_o_of(g), tmem + col_s_of(g) + ks * 8,
-                           tc::sdesc_sw128(vsm + ks * 2048, kBoxBytes, 1024), idesc_pv,
-                           (j > 0 || ks > 0) ? 1u : 0u);
-            };
-            bool alive = mbar_wait_bounded(bar(pQFull), 0, p.status) && wait_item(0);
-            if (alive) {
-                tc::fence_after_sync();
-                issue_s(0, 0);
-                issue_s(1, 0);
-                tc::commit(bar(pSlotEmpty + 0));  // K_0 read by both S MMAs
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                tc::mma_ss(tmem + col_s_of(g), qdesc + off, kdesc + off, idesc_s, kk > 0);
             }
-            for (int j = 0; j < n_tiles && alive; ++j) {
-                const bool more = j + 1 < n_tiles;
+            tc::commit(bar(pSFull + g));
+        };
+        auto issue_pv = [&](int g, int ri, bool first) {  // O_g (+)= P_g V, V in ring item ri
+            const uint64_t vdesc = tc::sdesc_sw128(slot_addr(ri), kBoxBytes, 1024);
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks)
+                mma_ts(tmem + col_o_of(g), tmem + col_s_of(g) + ks * 8,
+                       vdesc + uint64_t((ks * 2048) >> 4), idesc_pv,
+                       (!first || ks > 0) ? 1u : 0u);
+        };
+        bool alive = true;
+        int r = 0;   // ring items consumed so far
+        int tt = 0;  // KV tiles finished so far (S and P barrier phases)
+        for (int it = 0; alive && pair_item(p, it, w); ++it) {
+            const int n = w.n_tiles;
+            alive = mbar_wait_fast(bar(pQFull), it & 1, p.status) && wait_item(r);
+            if (!alive) break;
+            tc::fence_after_sync();
+            issue_s(0, r);
+            issue_s(1, r);
+            tc::commit(bar(pSlotEmpty + r % kRingSlots));  // K_0 read by both S MMAs
+            if (n == 1) tc::commit(bar(pQEmpty));
+            for (int j = 0; j < n && alive; ++j) {
+                const bool more = j + 1 < n;
+                const int rv = r + 2 * j + 1;  // V_j; K_{j+1} follows it
+                // the loads first (they land early), so that once P is ready
+                // only the fence and the issue remain
+                alive = wait_item(rv);
+                if (alive && more) alive = wait_item(rv + 1);
                 for (int g = 0; g < 2 && alive; ++g) {
-                    alive = mbar_wait_bounded(bar(pPFull + g), j & 1, p.status);
-                    if (alive && g == 0) alive = wait_item(2 * j + 1);  // V_j
-                    if (alive && g == 0 && more) alive = wait_item(2 * j + 2);  // K_{j+1}
+                    // P_g(0) of an item is written after the softmax threads
+                    // have read the previous item's O_g, so PV_g(0) may
+                    // overwrite it.
+                    alive = mbar_wait_fast(bar(pPFull + g), (tt + j) & 1, p.status);
                     if (!alive) break;
                     tc::fence_after_sync();
-                    issue_pv(g, j);
-                    if (g == 1) tc::commit(bar(pSlotEmpty + (2 * j + 1) % kRingSlots));  // V_j
+                    issue_pv(g, rv, j == 0);
+                    if (g == 1) tc::commit(bar(pSlotEmpty + rv % kRingSlots));  // done with V_j
                     if (more) {
-                        issue_s(g, j + 1);
-                        if (g == 1)
-                            tc::commit(bar(pSlotEmpty + (2 * j + 2) % kRingSlots));  // K_{j+1}
+                        issue_s(g, rv + 1);
+                        if (g == 1) {
+                            tc::commit(bar(pSlotEmpty + (rv + 1) % kRingSlots));  // K_{j+1}
+                            if (j + 2 == n) tc::commit(bar(pQEmpty));  // last S of the item
+                        }
                     } else {
                         tc::commit(bar(pODone + g));
                     }
                 }
             }
-            tc::commit(bar(pDrain));
-            mbar_wait_bounded(bar(pDrain), 0, p.status);
+            r += 2 * n;
+            tt += n;
         }
+        // No MMA may still run when the tensor memory is freed.
+        tc::commit(bar(pDrain));
+        mbar_wait_bounded(bar(pDrain), 0, p.status);
       }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
         // ------------------------------------------------ softmax warpgroups
         const int g = wg - 1;                 // 0: head h0, 1: head h0 + 1
         const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31
         const int row = quad * 32 + lane;
-        const int qg = qs + row;
         const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
         const uint32_t col_s = col_s_of(g), col_o = col_o_of(g);
-        float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
+        const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
         bool alive = true;
-        for (int j = 0; j < n_tiles && alive; ++j) {
-            alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pSFull + g), j & 1, p.status));
+        int tt = 0;  // KV tiles finished so far, over all work items
+        for (int it = 0; alive && pair_item(p, it, w); ++it) {
+            const int qg = w.qs + row;
+            float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
+            for (int j = 0; j < w.n_tiles && alive; ++j) {
+                alive = __all_sync(0xffffffffu,
+                                   mbar_wait_fast(bar(pSFull + g), (tt + j) & 1, p.status));
+                if (!alive) break;
+                tc::fence_after_sync();
+                float sv[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(lane_base + col_s + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[i]);
+                }
+                tc::tmem_wait_ld();
+
+                const int ks = j * BN, ke = min(ks + BN, p.S_kv);
+                const bool masked =
+                    (p.causal && tile_class(w.qs, w.qe, ks, ke) == kTilePartial) || (ke - ks < BN);
+                if (masked) {
+                    const int lim = (p.causal ? min(qg, p.S_kv - 1) : p.S_kv - 1) - ks;
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) sv[c] = c <= lim ? sv[c] : -INFINITY;
+                }
+                float mx;
+                {
+                    float mm[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mm[i] = fmaxf(sv[i], sv[8 + i]);
+#pragma unroll
+                    for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mm[i] = fmax3(mm[i], sv[c + i], sv[c + 8 + i]);
+                    mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]),
+                               fmaxf(mm[6], mm[7]));
+                }
+                const float m_new = fmaxf(m_run, mx * p.scale_log2);
+                const bool need = m_new > m_run + kRescaleThreshold;
+                const float corr = need ? fast_exp2(m_run - m_new) : 1.f;
+                const float m_use = need ? m_new : m_run;
+                m_run = m_use;
+                // O is complete here: this tile's S MMA was issued after the
+                // previous P.V, and tcgen05 MMAs complete in order.
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    const uint64_t corr2 = f2pack(corr, corr);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tc::tmem_ld32(lane_base + col_o + c * 32, r);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float a0, a1;
+                            f2unpack(fmul2(f2pack(__uint_as_float(r[2 * i]),
+                                                  __uint_as_float(r[2 * i + 1])),
+                                           corr2),
+                                     a0, a1);
+                            r[2 * i] = __float_as_uint(a0);
+                            r[2 * i + 1] = __float_as_uint(a1);
+                        }
+                        tc::tmem_st32(lane_base + col_o + c * 32, r);
+                    }
+                }
+                // p = 2^(s*scale - m): sums of p and of bf16(p); P (bf16 pairs,
+                // lower key in the low half) over the first 64 columns of S.
+                const uint64_t n2 = f2pack(-m_use, -m_use);
+                uint64_t s2[4], b2[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) s2[u] = b2[u] = 0ull;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = half * 64 + 2 * i;
+                        float x0, x1;
+                        f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), c2, n2), x0, x1);
+                        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                        s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
+                        pk[i] = pack_bf16x2(e0, e1);
+                        b2[i & 3] = fadd2(b2[i & 3], f2pack(__uint_as_float(pk[i] << 16),
+                                                            __uint_as_float(pk[i] & 0xFFFF0000u)));
+                    }
+                    tc::tmem_st32(lane_base + col_s + half * 32, pk);
+                }
+                {
+                    float t[8], tb[8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
+                        f2unpack(b2[u], tb[2 * u], tb[2 * u + 1]);
+                    }
+                    l_run = l_run * corr +
+                            (((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7])));
+                    lb_run = lb_run * corr + (((tb[0] + tb[1]) + (tb[2] + tb[3])) +
+                                              ((tb[4] + tb[5]) + (tb[6] + tb[7])));
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(pPFull + g));
+            }
+            if (!alive) break;
+
+            // ---- epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2. Every
+            // read of O_g completes (wait::ld) before this warp's next P
+            // arrive, which is what lets the next item's PV_g(0) overwrite O_g.
+            alive = __all_sync(0xffffffffu, mbar_wait_fast(bar(pODone + g), it & 1, p.status));
             if (!alive) break;
             tc::fence_after_sync();
-            float sv[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32(lane_base + col_s + c * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[i]);
-            }
-            tc::tmem_wait_ld();
-
-            const int ks = j * BN, ke = min(ks + BN, p.S_kv);
-            const bool masked =
-                (p.causal && tile_class(qs, qe, ks, ke) == kTilePartial) || (ke - ks < BN);
-            if (masked) {
-                const int lim = (p.causal ? min(qg, p.S_kv - 1) : p.S_kv - 1) - ks;
-#pragma unroll
-                for (int c = 0; c < BN; ++c) sv[c] = c <= lim ? sv[c] : -INFINITY;
-            }
-            float mx;
-            {
-                float mm[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mm[i] = fmaxf(sv[i], sv[8 + i]);
-#pragma unroll
-                for (int c = 16; c < BN; c += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mm[i] = fmax3(mm[i], sv[c + i], sv[c + 8 + i]);
-                mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]),
-                           fmaxf(mm[6], mm[7]));
-            }
-            const float m_new = fmaxf(m_run, mx * p.scale_log2);
-            const bool need = m_new > m_run + kRescaleThreshold;
-            const float corr = need ? fast_exp2(m_run - m_new) : 1.f;
-            const float m_use = need ? m_new : m_run;
-            m_run = m_use;
-            // O is complete here: this tile's S MMA was issued after the
-            // previous P.V, and tcgen05 MMAs complete in order.
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                const uint64_t corr2 = f2pack(corr, corr);
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tc::tmem_ld32(lane_base + col_o + c * 32, r);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float a0, a1;
-                        f2unpack(fmul2(f2pack(__uint_as_float(r[2 * i]),
-                                              __uint_as_float(r[2 * i + 1])),
-                                       corr2),
-                                 a0, a1);
-                        r[2 * i] = __float_as_uint(a0);
-                        r[2 * i + 1] = __float_as_uint(a1);
-                    }
-                    tc::tmem_st32(lane_base + col_o + c * 32, r);
-                }
-            }
-            // p = 2^(s*scale - m): sums of p and of bf16(p); P (bf16 pairs,
-            // lower key in the low half) over the first 64 columns of S.
-            const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
-            const uint64_t n2 = f2pack(-m_use, -m_use);
-            uint64_t s2[4], b2[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) s2[u] = b2[u] = 0ull;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = half * 64 + 2 * i;
-                    float x0, x1;
-                    f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), c2, n2), x0, x1);
-                    const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-                    s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
-                    pk[i] = pack_bf16x2(e0, e1);
-                    b2[i & 3] = fadd2(b2[i & 3], f2pack(__uint_as_float(pk[i] << 16),
-                                                        __uint_as_float(pk[i] & 0xFFFF0000u)));
-                }
-                tc::tmem_st32(lane_base + col_s + half * 32, pk);
-            }
-            {
-                float t[8], tb[8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
-                    f2unpack(b2[u], tb[2 * u], tb[2 * u + 1]);
-                }
-                l_run = l_run * corr +
-                        (((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7])));
-                lb_run = lb_run * corr +
-                         (((tb[0] + tb[1]) + (tb[2] + tb[3])) + ((tb[4] + tb[5]) + (tb[6] + tb[7])));
-            }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(pPFull + g));
-        }
-
-        // ---- epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
-        if (alive)
-            alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pODone + g), 0, p.status));
-        if (alive) {
-            tc::fence_after_sync();
-            const bool valid = m0 + row < p.T_q;
+            const bool valid = w.m0 + row < p.T_q;
             const float inv = 1.f / lb_run;
-            const size_t orow = (size_t(b) * p.H_q + h0 + g) * p.T_q + m0 + row;
+            const size_t orow = (size_t(w.b) * p.H_q + w.h0 + g) * p.T_q + w.m0 + row;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -686,20 +749,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + c * 32);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 7]) * inv);
-                        dst[v4] = w;
+                        uint4 o4;
+                        o4.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv,
+                                           __uint_as_float(r[v4 * 8 + 1]) * inv);
+                        o4.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv,
+                                           __uint_as_float(r[v4 * 8 + 3]) * inv);
+                        o4.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv,
+                                           __uint_as_float(r[v4 * 8 + 5]) * inv);
+                        o4.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv,
+                                           __uint_as_float(r[v4 * 8 + 7]) * inv);
+                        dst[v4] = o4;
                     }
                 }
             }
             if (valid && p.lse) p.lse[orow] = (m_run + __log2f(l_run)) * kLn2;
+            tt += w.n_tiles;
         }
     }
 
@@ -778,9 +842,12 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     const bool pair = prm.G % 2 == 0;
     const int64_t items = int64_t(prm.n_mblocks) * B * (pair ? H_q / 2 : H_q);
     if (items > 0x7fffffff) return GQA_ERR_UNSUPPORTED;
-    if (pair)
-        prefill_pair_kernel<<<dim3(unsigned(items)), kPairThreads, kPairSmemBytes, stream>>>(
+    if (pair) {
+        // persistent: one CTA per SM (at most one per work item)
+        const int ctas = int(items < int64_t(num_sms()) ? items : int64_t(num_sms()));
+        prefill_pair_kernel<<<dim3(unsigned(ctas)), kPairThreads, kPairSmemBytes, stream>>>(
             tq, tk, tv, prm);
+    }
     else
         prefill_kernel<<<dim3(unsigned(items)), kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
@@ -793,3 +860,17 @@ extern "C" int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint
     return gqa_attn_prefill_ex(q, k, v, o, lse, B, 64, 8, 128, T_q, S_kv, q_offset, causal,
                                scale, stream);
 }
+
+#ifdef GQA_TRACE
+extern "C" int gqa_attn_trace_dump_prefill(void* host, size_t bytes, int clear) {
+    if (bytes > sizeof(gqa::g_trace)) bytes = sizeof(gqa::g_trace);
+    if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(host, gqa::g_trace, bytes) != cudaSuccess) return GQA_ERR_CUDA;
+    if (clear) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, gqa::g_trace) != cudaSuccess) return GQA_ERR_CUDA;
+        if (cudaMemset(p, 0, sizeof(gqa::g_trace)) != cudaSuccess) return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+#endif
