@@ -68,6 +68,7 @@ struct SplitParams {
     int B, H_q, H_kv, G, S_max, ns, L, n_groups;
     float scale_log2;         // scale * log2(e)
     int inject_timeout;       // test hook: block (0,0,0) withholds its first copy
+    int trace_row0;           // first timeline row of this launch (trace builds only)
 };
 
 template <int D, int TILE_T, int STAGES, int WARPS>
@@ -160,12 +161,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // Let a dependent combine grid get scheduled while this one streams (it
     // waits for our results with griddepcontrol.wait before reading anything).
     pdl_launch_dependents();
-    [[maybe_unused]] const int blin = (b * gridDim.y + kv) * gridDim.x + s;
+    [[maybe_unused]] const int blin = p.trace_row0 + (b * gridDim.y + kv) * gridDim.x + s;
     if (threadIdx.x == 0) {
         GQA_TRACE_STAMP(blin, 0);
         unsigned smid;
         asm("mov.u32 %0, %%smid;" : "=r"(smid));
-        GQA_TRACE_VALUE(blin, 5, smid);
+        GQA_TRACE_VALUE(blin, 6, smid);
     }
 
     // ---- set-up that touches no global memory: it may overlap the previous
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     if constexpr (CS > 1) cluster_arrive_release();
 
     pdl_wait_primary();  // everything below may read what earlier kernels wrote
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 1);
 
     const int seqlen = load_seqlen(p.seqlens, b, p.S_max, p.status,
                                    s == 0 && kv == 0 && threadIdx.x == 0);
@@ -217,29 +219,33 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         const int tok0 = r.start + (warp + i * WARPS) * TILE_T;
         return tok0 + TILE_T <= r.end ? tok0 : r.end - TILE_T;
     };
-    auto issue = [&](int i) {
+    // A stage is 2 * kBoxes copies (K and V, 64 columns each). Lane 0 arms
+    // the stage's barrier, then each copy goes out from its own lane.
+    constexpr int kCopies = 2 * C::kBoxes;
+    static_assert(STAGES * kCopies <= 32, "one lane per copy of the first stages");
+    auto copy = [&](int i, int j) {  // copy j of tile i: K or V (j & 1), box j >> 1
         const int slot = i % STAGES;
-        const uint32_t bar = smem_u32(&bars[slot]);
-        const uint32_t kdst = smem_u32(ring + slot * C::kStageBytes);
-        const uint32_t vdst = kdst + C::kKBytes;
-        const int y = tile_y(i);
-        mbar_arrive_expect_tx(bar, C::kStageBytes);
-#pragma unroll
-        for (int h = 0; h < C::kBoxes; ++h) {
-            tma_load_3d(kdst + h * C::kBoxBytes, &tmap_k, h * 64, y, zc, bar, policy);
-            tma_load_3d(vdst + h * C::kBoxBytes, &tmap_v, h * 64, y, zc, bar, policy);
-        }
+        const uint32_t dst = smem_u32(ring + slot * C::kStageBytes) + (j & 1) * C::kKBytes +
+                             (j >> 1) * C::kBoxBytes;
+        tma_load_3d(dst, (j & 1) ? &tmap_v : &tmap_k, (j >> 1) * 64, tile_y(i), zc,
+                    smem_u32(&bars[slot]), policy);
+    };
+    auto issue = [&](int i) {  // the whole warp
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars[i % STAGES]), C::kStageBytes);
+        __syncwarp();
+        if (lane < kCopies) copy(i, lane);
     };
 
     // Test hook: the first block withholds its first copy, so its first wait
     // runs out and reports kStatusTimeout (nothing faults, nothing hangs).
     const bool withhold = p.inject_timeout && s == 0 && kv == 0 && b == 0 && warp == 0;
-    int issued = 0;
-    if (lane == 0) {
-        for (; issued < STAGES && issued < my_n; ++issued)
-            if (!(withhold && issued == 0)) issue(issued);
-    }
-    issued = __shfl_sync(0xffffffffu, issued, 0);
+    const int issued0 = min(STAGES, my_n);
+    if (lane == 0)
+        for (int i = withhold ? 1 : 0; i < issued0; ++i)
+            mbar_arrive_expect_tx(smem_u32(&bars[i]), C::kStageBytes);
+    __syncwarp();
+    if (lane < issued0 * kCopies && !(withhold && lane < kCopies)) copy(lane / kCopies, lane % kCopies);
+    int issued = issued0;
 
     // q^T as the B operand (k = head dim, n = query head g of this group).
     uint32_t qf[C::kKC][2];
@@ -269,7 +275,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             alive = __all_sync(0xffffffffu, alive);  // keep the warp's control flow uniform
             if (alive) waited = i + 1;                // copies observed complete so far
         }
-        if (i == 0 && threadIdx.x == 0) GQA_TRACE_STAMP(blin, 1);
+        if (i == 0 && threadIdx.x == 0) GQA_TRACE_STAMP(blin, 2);
         const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
         const int tok0 = r.start + (warp + i * WARPS) * TILE_T;
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
 
         __syncwarp();
-        if (lane == 0 && alive && issued < my_n) issue(issued);
+        if (alive && issued < my_n) issue(issued);
         if (alive && issued < my_n) ++issued;
     }
     // A wait that ran out may leave copies in flight: wait for them (bounded)
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 2);
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 3);
 
     // ---- level 2a: the other warps hand their partials to warp 0, which
     // merges them fragment by fragment in registers (warp order fixed).
@@ -465,7 +471,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
     }
 
-    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 4);
     if constexpr (CS > 1) {
         // ---- level 2b. Cluster barrier, phase 1: each thread's stores are
         // released by its arrive and acquired by every wait, so all records
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         // memory after this point, so none can outlive a store aimed at it.
         cluster_arrive_release();
         cluster_wait_acquire();
-        if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 6);
+        if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 4);
         // Per owned head, warp 0 alone: lane q holds sender q's (m, l), the
         // weights come from two warp reductions, and each lane folds the CS
         // records over its D/32 dims with vector loads (rank order fixed).
@@ -504,9 +509,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 for (int e = 0; e < kPer; ++e) emit(p, row, gi, lane * kPer + e, D, mstar, lsum, o[e]);
             }
         }
-        if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 7);
     }
-    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 3);
+    if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 5);
 }
 
 struct CombineParams {
@@ -769,6 +773,12 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
             sp.inject_timeout = 1;
             break;
         }
+#ifdef GQA_TRACE
+    static int trace_row = 0;  // consecutive launches get consecutive timeline rows
+    if (trace_row + ns * H_kv * B > kTraceCombineBase) trace_row = 0;
+    sp.trace_row0 = trace_row;
+    trace_row += ns * H_kv * B;
+#endif
     return d == 128 ? launch<128>(sp, cs, tk, tv, stream) : launch<64>(sp, cs, tk, tv, stream);
 }
 
