@@ -56,6 +56,10 @@ constexpr int kMaxG = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+#ifndef GQA_DEC_WARM_TILES
+#define GQA_DEC_WARM_TILES 3  // tiles per warp warmed in L2 before griddepcontrol.wait
+#endif
+
 struct SplitParams {
     const uint16_t* q;        // [B, H_q, D]
     const int32_t* seqlens;   // [B] or null
@@ -69,6 +73,7 @@ struct SplitParams {
     float scale_log2;         // scale * log2(e)
     int inject_timeout;       // test hook: block (0,0,0) withholds its first copy
     int trace_row0;           // first timeline row of this launch (trace builds only)
+    int warm_l2;              // the grid fits in one wave: warm L2 before griddepcontrol.wait
 };
 
 template <int D, int TILE_T, int STAGES, int WARPS>
@@ -158,9 +163,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
 
-    // Let a dependent combine grid get scheduled while this one streams (it
-    // waits for our results with griddepcontrol.wait before reading anything).
-    pdl_launch_dependents();
     [[maybe_unused]] const int blin = p.trace_row0 + (b * gridDim.y + kv) * gridDim.x + s;
     if (threadIdx.x == 0) {
         GQA_TRACE_STAMP(blin, 0);
@@ -168,6 +170,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         asm("mov.u32 %0, %%smid;" : "=r"(smid));
         GQA_TRACE_VALUE(blin, 6, smid);
     }
+
+    // With more than one group per row the combine kernel follows: let it be
+    // scheduled now (it waits for this grid before reading anything).
+    if (p.n_groups > 1) pdl_launch_dependents();
 
     // ---- set-up that touches no global memory: it may overlap the previous
     // kernel in the stream (programmatic dependent launch).
@@ -189,6 +195,27 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // Cluster barrier, phase 0: every CTA of the cluster is running before any
     // of them stores into another's shared memory (arrive now, wait later).
     if constexpr (CS > 1) cluster_arrive_release();
+
+    // Warm L2 with this warp's first tiles while the previous kernel in
+    // the stream finishes its merge (that kernel lets this grid launch once
+    // its own K/V streams are done). The row length read here may be stale:
+    // it only chooses what to warm, and every load below uses the length
+    // read after griddepcontrol.wait.
+    if (p.warm_l2 && s < p.ns) {
+        int hint = p.seqlens ? *reinterpret_cast<const volatile int32_t*>(p.seqlens + b) : p.S_max;
+        hint = hint < 0 ? 0 : (hint > p.S_max ? p.S_max : hint);
+        const SplitRange rh = split_range(p.L, s, hint);
+        const int nt = (rh.end - rh.start + TILE_T - 1) / TILE_T;
+        const int mine = warp < nt ? (nt - warp + WARPS - 1) / WARPS : 0;
+        constexpr int kPf = 2 * C::kBoxes;  // K and V boxes of one tile
+        static_assert(GQA_DEC_WARM_TILES * kPf <= 32, "one lane per prefetch");
+        if (lane < min(GQA_DEC_WARM_TILES, mine) * kPf) {
+            const int i = lane / kPf, j = lane % kPf;
+            const int tok0 = rh.start + (warp + i * WARPS) * TILE_T;
+            const int y = tok0 + TILE_T <= rh.end ? tok0 : rh.end - TILE_T;
+            tma_prefetch_l2_3d((j & 1) ? &tmap_v : &tmap_k, (j >> 1) * 64, y, b * p.H_kv + kv);
+        }
+    }
 
     pdl_wait_primary();  // everything below may read what earlier kernels wrote
     if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 1);
@@ -373,6 +400,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
     if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 3);
+    // This CTA's K/V stream is done: the next kernel in the stream may launch
+    // now and warm L2 while this grid merges (it reads nothing this grid
+    // writes before its griddepcontrol.wait). A combine kernel that follows
+    // was allowed to launch at the start.
+    if (p.n_groups == 1) pdl_launch_dependents();
 
     // ---- level 2a: the other warps hand their partials to warp 0, which
     // merges them fragment by fragment in registers (warp order fixed).
@@ -767,6 +799,7 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.ns = ns;
     sp.L = split_len(S_max, ns);
     sp.n_groups = ns / cs;
+    sp.warm_l2 = int64_t(ns) * H_kv * B <= num_sms() ? 1 : 0;  // a single wave
     sp.scale_log2 = scale * kLog2e;
     for (int n = g_inject_timeout.load(); n > 0; n = g_inject_timeout.load())
         if (g_inject_timeout.compare_exchange_weak(n, n - 1)) {
@@ -959,6 +992,7 @@ extern "C" int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, con
     sp.ns = ns;
     sp.L = gqa::split_len(S_max, ns);
     sp.n_groups = ns / cs;
+    sp.warm_l2 = int64_t(ns) * H_kv * B <= num_sms() ? 1 : 0;  // a single wave
     sp.scale_log2 = scale * kLog2e;
     return d == 128 ? launch<128>(sp, cs, tk, tv, stream) : launch<64>(sp, cs, tk, tv, stream);
 }
