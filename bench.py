@@ -284,9 +284,9 @@ def run_ours(args, rank, world, local_rank):
         api.prefill(qp, kp, vp, q_offset=p.q_offset, causal=True, out=op, lse=lsep)
 
     splits_active = sum(math.ceil(int(s) / math.ceil(w.S_max / ns)) for s in sl0.tolist())
-    # the combine kernel runs only when a row spans several 16-split clusters,
-    # i.e. exactly when the call needs workspace
-    combine = api.gqa_attn_decode_workspace_size(w.B, w.H_q, w.d, ns) > 0
+    # the combine kernel runs only when a row spans several clusters
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    combine = ns // api.gqa_attn_decode_cluster_size(w.B, w.H_kv, ns, sms) > 1
     launches_decode = LAYERS * (1 + (1 if combine else 0))
     launches_prefill = 1 if have_prefill else 0
 
@@ -320,6 +320,18 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     clk = clocks.stop()
     api.check(stream)
+
+    # the same 80 decode calls as plain launches (no graph), after the timed
+    # region, for reference
+    with torch.cuda.stream(stream):
+        pl0, pl1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        pl0.record(stream)
+        for _ in range(3):
+            decode_layers()
+        pl1.record(stream)
+    stream.synchronize()
+    api.check(stream)
+    plain_call_us = pl0.elapsed_time(pl1) * 1e3 / (3 * LAYERS)
 
     dec_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
     pre_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
@@ -362,6 +374,7 @@ def run_ours(args, rank, world, local_rank):
         "decode": {"kv_GBps": value, "pct_of_8TBps": 100 * dec_gbs_rank / NOMINAL_HBM_GBS,
                    "pct_of_measured_hbm": 100 * dec_gbs_rank / hbm_peak,
                    "us_per_layer_call": dec_call_s * 1e6,
+                   "plain_loop_us_per_layer_call": plain_call_us,
                    "tok_per_s_one_layer": w.B / dec_call_s,
                    "tok_per_s_80_layers": w.B / (dec_call_s * LAYERS)},
         "prefill": None if not have_prefill else {
@@ -483,7 +496,8 @@ def run_reference(args, rank, world):
             "config": {"workload": f"{LAYERS} x llama70b_decode_b1_s8192 decode (graph) + "
                                    "llama70b_causal_prefill_b1_t8192"},
             "prefill": {"TFLOPS": pre},
-            "cpu_baseline": {"value": dec, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": dec, "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(),
+                             "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": dec, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -584,7 +598,7 @@ def main():
             cb = cpu_oracle_sample(args.cpu_seconds)[0]
             res["cpu_baseline"] = {
                 "value": cb["decode_gbs"], "unit": "GB/s", "cores": cb["threads"],
-                "kind": "oracle",
+                "host_cores": os.cpu_count(), "kind": "oracle",
                 "sample": f"{cb['decode_rows']} query-head rows of the 8K decode in "
                           f"{cb['decode_s']:.1f}s (fp64 oracle, 1 thread); prefill rows: "
                           f"{cb['prefill_tflops']:.2e} TFLOP/s over {cb['prefill_rows']} rows",

@@ -646,19 +646,13 @@ constexpr int kTileT = GQA_DEC_TILE_T, kStages = GQA_DEC_STAGES, kWarps = GQA_DE
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Cluster size for a grid of `ctas` CTAs with ns splits per row: the largest
-// of 16, 8, 4, 2 dividing ns, else 1. A grid of more than one wave takes at
-// most 8: smaller clusters fill the SMs that finished CTAs free more evenly
-// (ragged 128K decode on GB300: 141 us with clusters of 16, 132 us with 8).
-int cluster_size_for(int ns, int64_t ctas) {
-    const int max_cs = ctas != INT64_MAX && ctas <= num_sms() ? 16 : 8;
-    for (int cs : {16, 8, 4, 2})
-        if (cs <= max_cs && ns % cs == 0) return cs;
-    return 1;
-}
+// Cluster size of a launch on this device (the rule is decode_cluster_size in
+// plan.cuh; ragged 128K decode on GB300: 141 us with clusters of 16, 132 us
+// with 8).
+int cluster_size_for(int ns, int64_t ctas) { return decode_cluster_size(ns, ctas, num_sms()); }
 // The multi-wave choice: its clusters are never larger, so its workspace is
 // never smaller.
-int max_groups_cluster_size(int ns) { return cluster_size_for(ns, INT64_MAX); }
+int max_groups_cluster_size(int ns) { return decode_cluster_size(ns, INT64_MAX, 1); }
 
 struct WsLayout {
     size_t o_off, m_off, l_off, total;

@@ -45,6 +45,11 @@ extern "C" int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms)
     return int(ns);
 }
 
+extern "C" int gqa_attn_decode_cluster_size(int B, int H_kv, int num_splits, int num_sms) {
+    if (B <= 0 || H_kv <= 0 || num_splits <= 0 || num_sms <= 0) return GQA_ERR_INVALID_ARG;
+    return gqa::decode_cluster_size(num_splits, int64_t(num_splits) * H_kv * B, num_sms);
+}
+
 extern "C" int gqa_attn_split_bounds(int S_max, int num_splits, int seqlen, int32_t* starts,
                                      int32_t* ends) {
     if (S_max <= 0 || num_splits <= 0 || seqlen < 0 || seqlen > S_max || !starts || !ends)

@@ -49,4 +49,15 @@ GQA_HD int tile_class(int qs, int qe, int ks, int ke) {
     return kTilePartial;
 }
 
+// Cluster size of a decode launch with ns splits per row and `ctas` CTAs in
+// all: the largest of 16, 8, 4, 2 dividing ns, else 1; at most 8 when the
+// grid needs more than one wave (more CTAs than the num_sms SMs), because
+// smaller clusters fill the SMs that finished CTAs free more evenly.
+inline int decode_cluster_size(int ns, int64_t ctas, int num_sms) {
+    const int max_cs = ctas <= int64_t(num_sms) ? 16 : 8;
+    for (int cs : {16, 8, 4, 2})
+        if (cs <= max_cs && ns % cs == 0) return cs;
+    return 1;
+}
+
 }  // namespace gqa

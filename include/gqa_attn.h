@@ -167,6 +167,14 @@ int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * >= 1, or GQA_ERR_INVALID_ARG. */
 int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
 
+/* Cluster size a decode launch uses on a GPU with num_sms SMs: the largest of
+ * 16, 8, 4, 2 that divides num_splits (else 1), at most 8 when the grid of
+ * num_splits * H_kv * B CTAs needs more than one wave (more CTAs than SMs).
+ * The splits of one cluster are merged on chip; a row spanning several
+ * clusters is finished by the combine kernel. Returns the size, or
+ * GQA_ERR_INVALID_ARG. */
+int gqa_attn_decode_cluster_size(int B, int H_kv, int num_splits, int num_sms);
+
 /* Fills starts[s], ends[s] (s < num_splits) with the decode split plan above
  * for one row of length seqlen (0 <= seqlen <= S_max). */
 int gqa_attn_split_bounds(int S_max, int num_splits, int seqlen,

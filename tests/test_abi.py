@@ -113,6 +113,25 @@ def test_pick_num_splits_bit_exact_and_properties(L):
     assert api.gqa_attn_pick_num_splits(0, 8, 8192, 152) == api.GQA_ERR_INVALID_ARG
 
 
+def test_decode_cluster_size(L):
+    # largest of 16, 8, 4, 2 dividing the split count; at most 8 once the grid
+    # (splits x KV heads x batch) has more CTAs than SMs
+    cases = [((1, 8, 16, 152), 16),    # 8K decode: 128 CTAs, one wave
+             ((1, 8, 19, 152), 1),     # prime split count: no clusters
+             ((1, 8, 6, 152), 2),
+             ((1, 8, 12, 152), 4),
+             ((1, 8, 24, 152), 8),     # 192 CTAs: more than one wave
+             ((4, 8, 128, 152), 8),    # ragged 128K batch
+             ((3, 2, 32, 152), 8),
+             ((1, 2, 64, 152), 16),    # exactly 128 CTAs
+             ((1, 19, 8, 152), 8),     # exactly 152 CTAs
+             ((1, 1, 1, 152), 1)]
+    for args, cs in cases:
+        assert api.gqa_attn_decode_cluster_size(*args) == cs, args
+    for bad in ((0, 8, 16, 152), (1, 0, 16, 152), (1, 8, 0, 152), (1, 8, 16, 0)):
+        assert api.gqa_attn_decode_cluster_size(*bad) == api.GQA_ERR_INVALID_ARG
+
+
 def test_workspace_size(L):
     assert api.gqa_attn_decode_workspace_size(1, 64, 128, 1) == 0
     n = api.gqa_attn_decode_workspace_size(1, 64, 128, 19)
