@@ -11,6 +11,7 @@ from .gqa_oracle import (  # noqa: F401
     TILE_ALL_PAST,
     TILE_PARTIAL,
     attention,
+    attention_ring,
     attention_rows,
     combine_partials,
     finalize,
@@ -18,6 +19,9 @@ from .gqa_oracle import (  # noqa: F401
     lse_merge,
     online_softmax_sweep,
     prefill_tile_classes,
+    ring_slot,
+    ring_visible_tokens,
+    ring_write,
     split_bounds,
     split_len,
     split_partials,

@@ -328,3 +328,76 @@ def prefill_tile_classes(T_q: int, S_kv: int, q_offset: int, block_m: int, block
         for j in range(nn):
             out[i, j] = tile_class(qs, qe, j * block_n, min((j + 1) * block_n, S_kv))
     return out
+
+
+# ---------------------------------------------------------------------------
+# Hard-capped ring-buffer KV cache with attention sinks.
+#
+# Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §2 item 4 (the KV
+# cache is initialised with a fixed max_tokens and never grows) and §4 item 2
+# (once the ring wraps, the oldest entries are overwritten under an
+# attention-sink + local-window policy). Readings where the page is silent:
+#   * the first n_sink tokens of a row are the sinks and are never
+#     overwritten; every later token overwrites the oldest non-sink token, so
+#     the cache holds the sinks plus the last (capacity - n_sink) tokens;
+#   * a decode step attends to exactly the tokens the cache holds.
+# Everything below works at the token level (which token ids are visible,
+# which slot a token id lands in), never at the kernel's level.
+# ---------------------------------------------------------------------------
+
+
+def ring_slot(t: int, capacity: int, n_sink: int) -> int:
+    """Cache slot of token t: sinks keep their own slot, the rest cycle."""
+    assert 0 <= n_sink < capacity and t >= 0
+    if t < n_sink:
+        return t
+    return n_sink + (t - n_sink) % (capacity - n_sink)
+
+
+def ring_visible_tokens(seqlen: int, capacity: int, n_sink: int):
+    """Token ids a row of `seqlen` tokens keeps: the sinks, then the window."""
+    assert 0 <= n_sink < capacity and seqlen >= 0
+    sinks = list(range(min(seqlen, n_sink)))
+    window = capacity - n_sink
+    recent_start = max(n_sink, seqlen - window)
+    return sinks + list(range(recent_start, seqlen))
+
+
+def ring_write(stream, seqlen: int, capacity: int, n_sink: int, fill=np.nan):
+    """Replays the writes of tokens 0 .. seqlen-1 of `stream` ([T, ...], T >=
+    seqlen) into a cache of `capacity` slots, one token at a time in order;
+    slots never written hold `fill`. Returns the cache [capacity, ...]."""
+    stream = np.asarray(stream)
+    cache = np.full((capacity,) + stream.shape[1:], fill, dtype=np.float64)
+    for t in range(seqlen):
+        cache[ring_slot(t, capacity, n_sink)] = stream[t]
+    return cache
+
+
+def attention_ring(q, k_stream, v_stream, *, scale: float, seqlens, capacity: int,
+                   n_sink: int):
+    """Decode attention under the sink + window policy, by its definition:
+    softmax over the visible tokens of each row's token stream.
+
+    q: [B, H_q, d]; k_stream, v_stream: [B, H_kv, T, d] (every token the row
+    has produced, T >= max seqlens). Returns O [B, H_q, d], lse [B, H_q].
+    """
+    q = to_f64(q)
+    B, H_q, d = q.shape
+    H_kv = k_stream.shape[1]
+    G = H_q // H_kv
+    O = np.zeros((B, H_q, d))
+    lse = np.zeros((B, H_q))
+    for b in range(B):
+        ids = ring_visible_tokens(int(seqlens[b]), capacity, n_sink)
+        for h in range(H_q):
+            kv = h // G
+            if not ids:
+                O[b, h], lse[b, h] = 0.0, NEG_INF
+                continue
+            Kr = to_f64(k_stream[b, kv, ids])
+            Vr = to_f64(v_stream[b, kv, ids])
+            scores = (Kr @ q[b, h])[None, :] * scale
+            o, l_, _ = _softmax_attend(scores, Vr)
+            O[b, h], lse[b, h] = o[0], l_[0]
+    return O, lse
