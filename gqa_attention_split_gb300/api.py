@@ -38,6 +38,8 @@ _SIGNATURES = {
                                 _P]),
     "gqa_attn_decode_workspace_size": (_S, [_I, _I, _I, _I]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "gqa_attn_ring_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gqa_attn_decode_ring": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_prefill_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_pick_num_splits": (_I, [_I, _I, _I, _I]),
@@ -237,6 +239,68 @@ def decode(q, k, v, seqlens=None, *, num_splits: int = 0, scale: float | None = 
                                 _ptr(workspace), workspace.numel(), st)
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_attn_decode")
+    return out, lse
+
+
+def gqa_attn_ring_append(k_cache, v_cache, k_new, v_new, positions, B, H_kv, d, capacity, n_sink,
+                         stream):
+    return lib().gqa_attn_ring_append(k_cache, v_cache, k_new, v_new, positions, B, H_kv, d,
+                                      capacity, n_sink, stream)
+
+
+def gqa_attn_decode_ring(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, capacity, n_sink, scale,
+                         num_splits, stream):
+    return lib().gqa_attn_decode_ring(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, capacity,
+                                      n_sink, scale, num_splits, stream)
+
+
+def ring_append(k_cache, v_cache, k_new, v_new, positions, *, n_sink: int, stream=None):
+    """Writes each row's newest token into its ring slot. k_cache/v_cache
+    [B,H_kv,capacity,d] bf16 CUDA; k_new/v_new [B,H_kv,d]; positions int32 [B]
+    (the new token's index in its row)."""
+    import torch
+
+    _check_cuda_bf16("k_cache", k_cache, 4)
+    _check_cuda_bf16("v_cache", v_cache, 4)
+    _check_cuda_bf16("k_new", k_new, 3)
+    _check_cuda_bf16("v_new", v_new, 3)
+    B, H_kv, capacity, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape != (B, H_kv, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new, v_new must be [B, H_kv, d] matching the caches")
+    if positions.dtype != torch.int32 or not positions.is_cuda or positions.numel() != B:
+        raise TypeError("positions must be an int32 CUDA tensor of B elements")
+    rc = gqa_attn_ring_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                              _ptr(positions), B, H_kv, d, capacity, n_sink, _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_ring_append")
+
+
+def decode_ring(q, k, v, seqlens, *, n_sink: int, num_splits: int = 0,
+                scale: float | None = None, out=None, lse=None, stream=None):
+    """Decode over a ring-buffer cache with attention sinks: k/v
+    [B,H_kv,capacity,d]; seqlens int32 [B] counts every token each row has
+    produced (it may exceed capacity). Returns (o, lse) as ``decode``."""
+    import torch
+
+    _check_cuda_bf16("q", q, 3)
+    _check_cuda_bf16("k", k, 4)
+    _check_cuda_bf16("v", v, 4)
+    B, H_q, d = q.shape
+    H_kv, capacity = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H_kv, capacity, d] matching q")
+    if seqlens.dtype != torch.int32 or not seqlens.is_cuda or seqlens.numel() != B:
+        raise TypeError("seqlens must be an int32 CUDA tensor of B elements")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = gqa_attn_decode_ring(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seqlens),
+                              B, H_q, H_kv, d, capacity, n_sink, sc, num_splits,
+                              _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_decode_ring")
     return out, lse
 
 

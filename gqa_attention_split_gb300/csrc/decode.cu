@@ -75,6 +75,7 @@ struct SplitParams {
     int inject_timeout;       // test hook: block (0,0,0) withholds its first copy
     int trace_row0;           // first timeline row of this launch (trace builds only)
     int warm_l2;              // the grid fits in one wave: warm L2 before griddepcontrol.wait
+    int ring;                 // ring-buffer cache: a row longer than S_max keeps S_max slots
 };
 
 template <int D, int TILE_T, int STAGES, int WARPS>
@@ -112,8 +113,9 @@ __device__ __forceinline__ void pdl_wait_primary() {
 }
 
 __device__ __forceinline__ int load_seqlen(const int32_t* seqlens, int b, int S_max,
-                                           unsigned* status, bool report) {
+                                           unsigned* status, bool report, bool ring) {
     int sl = seqlens ? seqlens[b] : S_max;
+    if (ring && sl > S_max) return S_max;  // every slot of a wrapped ring is live
     if (sl < 0 || sl > S_max) {
         if (report) atomicOr(status, kStatusBadSeqlen);
         sl = sl < 0 ? 0 : S_max;
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 1);
 
     const int seqlen = load_seqlen(p.seqlens, b, p.S_max, p.status,
-                                   s == 0 && kv == 0 && threadIdx.x == 0);
+                                   s == 0 && kv == 0 && threadIdx.x == 0, p.ring != 0);
     // A whole group beyond the row's end does nothing (uniform over the
     // cluster, so no CTA waits at a cluster barrier for one that left). With a
     // single group this can only be a row of length 0: O = 0, lse = -inf.
@@ -766,7 +768,7 @@ std::atomic<int> g_inject_timeout{0};
 
 int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse,
         const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max, float scale,
-        int ns, void* ws, size_t ws_bytes, cudaStream_t stream) {
+        int ns, void* ws, size_t ws_bytes, cudaStream_t stream, bool ring = false) {
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
     const int cs = cluster_size_for(ns, int64_t(ns) * H_kv * B);
@@ -802,6 +804,7 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.L = split_len(S_max, ns);
     sp.n_groups = ns / cs;
     sp.warm_l2 = int64_t(ns) * H_kv * B <= num_sms() ? 1 : 0;  // a single wave
+    sp.ring = ring ? 1 : 0;
     sp.scale_log2 = scale * kLog2e;
     for (int n = g_inject_timeout.load(); n > 0; n = g_inject_timeout.load())
         if (g_inject_timeout.compare_exchange_weak(n, n - 1)) {
@@ -871,6 +874,88 @@ extern "C" int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint1
     }
     return decode::run(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, ns, ws, bytes,
                        stream);
+}
+
+// ---------------------------------------------------------------------------
+// Hard-capped ring-buffer KV cache with attention sinks.
+//
+// Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §2 item 4 (the
+// cache has a fixed max_tokens) and §4 item 2 (a full ring overwrites its
+// oldest entry, keeping the attention sinks). Slots [0, n_sink) hold the
+// row's first n_sink tokens for good; token t >= n_sink lives in slot
+// n_sink + (t - n_sink) mod (capacity - n_sink). Softmax attention does not
+// depend on the order of its keys, so a decode step over such a cache is the
+// split-KV decode over its live slots: the first min(seqlen, capacity).
+
+namespace gqa {
+namespace decode {
+
+__global__ void __launch_bounds__(64)
+    ring_append_kernel(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
+                       const uint16_t* v_new, const int32_t* positions, int H_kv, int d,
+                       int capacity, int n_sink, unsigned* status) {
+    const int bk = blockIdx.x;  // b * H_kv + kv
+    const int t = positions[bk / H_kv];
+    if (t < 0) {
+        if (threadIdx.x == 0 && bk % H_kv == 0) atomicOr(status, kStatusBadSeqlen);
+        return;
+    }
+    const int slot = t < n_sink ? t : n_sink + (t - n_sink) % (capacity - n_sink);
+    const size_t dst = (size_t(bk) * capacity + slot) * d, src = size_t(bk) * d;
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {  // 16-byte chunks
+        reinterpret_cast<uint4*>(k_cache + dst)[i] = reinterpret_cast<const uint4*>(k_new + src)[i];
+        reinterpret_cast<uint4*>(v_cache + dst)[i] = reinterpret_cast<const uint4*>(v_new + src)[i];
+    }
+}
+
+}  // namespace decode
+}  // namespace gqa
+
+extern "C" int gqa_attn_ring_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
+                                    const uint16_t* v_new, const int32_t* positions, int B,
+                                    int H_kv, int d, int capacity, int n_sink,
+                                    cudaStream_t stream) {
+    if (!k_cache || !v_cache || !k_new || !v_new || !positions) return GQA_ERR_INVALID_ARG;
+    if (B < 0 || H_kv <= 0 || capacity < 1 || n_sink < 0 || n_sink >= capacity)
+        return GQA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+    if (int64_t(B) * H_kv >= (int64_t(1) << 31)) return GQA_ERR_UNSUPPORTED;
+    for (const void* ptr : {static_cast<const void*>(k_cache), static_cast<const void*>(v_cache),
+                            static_cast<const void*>(k_new), static_cast<const void*>(v_new)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return GQA_ERR_MISALIGNED;
+    if (B == 0) return GQA_OK;
+    unsigned* status = status_word();
+    if (!status) return GQA_ERR_CUDA;
+    decode::ring_append_kernel<<<dim3(unsigned(B * H_kv)), 64, 0, stream>>>(
+        k_cache, v_cache, k_new, v_new, positions, H_kv, d, capacity, n_sink, status);
+    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+extern "C" int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    uint16_t* o, float* lse, const int32_t* seqlens, int B,
+                                    int H_q, int H_kv, int d, int capacity, int n_sink,
+                                    float scale, int num_splits, cudaStream_t stream) {
+    if (n_sink < 0 || capacity < 1 || n_sink >= capacity || !seqlens) return GQA_ERR_INVALID_ARG;
+    int rc = decode::check_args(q, k, v, o, B, H_q, H_kv, d, capacity, scale, num_splits);
+    if (rc != GQA_OK) return rc;
+    if (B == 0) return GQA_OK;
+    int ns = num_splits;
+    if (ns == 0) {
+        const int sms = num_sms();
+        if (sms <= 0) return GQA_ERR_CUDA;
+        ns = gqa_attn_pick_num_splits(B, H_kv, capacity, sms);
+        if (ns < 1) return GQA_ERR_INVALID_ARG;
+    }
+    const size_t bytes = decode::ws_layout(B, H_q, d, ns,
+                                           decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
+                             .total;
+    void* ws = nullptr;
+    if (bytes > 0) {
+        ws = stream_workspace(stream, bytes);
+        if (!ws) return GQA_ERR_WORKSPACE;
+    }
+    return decode::run(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, capacity, scale, ns, ws, bytes,
+                       stream, /*ring=*/true);
 }
 
 #ifdef GQA_TRACE

@@ -135,6 +135,38 @@ int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t
                             int B, int H_q, int H_kv, int d, int S_max,
                             float scale, int num_splits, cudaStream_t stream);
 
+/* ------------------------------------------ ring-buffer cache with sinks --
+ * Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §2 item 4 (a KV
+ * cache of fixed max_tokens that never grows) and §4 item 2 (once it wraps,
+ * the oldest entry is overwritten under an attention-sink + local-window
+ * policy). The cache of each (batch row, KV head) has `capacity` slots:
+ * slots [0, n_sink) keep the row's first n_sink tokens for good, and token
+ * t >= n_sink lives in slot n_sink + (t - n_sink) % (capacity - n_sink), so a
+ * row that has produced seqlen tokens holds its sinks plus its last
+ * capacity - n_sink tokens (all of them while seqlen <= capacity).
+ * Requires 0 <= n_sink < capacity. */
+
+/* Writes each row's newest token into its slot: k_new/v_new [B, H_kv, d]
+ * (bf16, 16-byte aligned) go to k_cache/v_cache [B, H_kv, capacity, d] at
+ * the slot of token positions[b] (a device int32 [B]: the token's index, i.e.
+ * the row's length before this append). A negative position writes nothing
+ * and sets the status word's bad-length bit (gqa_attn_check reports
+ * GQA_ERR_DEVICE_BAD_INPUT). Async on `stream`; d in {64, 128}. */
+int gqa_attn_ring_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
+                         const uint16_t* v_new, const int32_t* positions, int B, int H_kv,
+                         int d, int capacity, int n_sink, cudaStream_t stream);
+
+/* Decode over such a cache: arguments as gqa_attn_decode with S_max =
+ * capacity, except that seqlens (required, device int32 [B]) counts every
+ * token the row has produced and may exceed capacity. The row attends to its
+ * live slots, min(seqlens[b], capacity) of them, which are exactly the sink
+ * and window tokens; a negative length is clamped to 0 and reported. Uses the
+ * library-owned workspace like gqa_attn_decode. */
+int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         uint16_t* o, float* lse, const int32_t* seqlens,
+                         int B, int H_q, int H_kv, int d, int capacity, int n_sink,
+                         float scale, int num_splits, cudaStream_t stream);
+
 /* --------------------------------------------------------------- prefill --
  * gqa_attn_prefill: T_q new queries at global positions q_offset + t against
  * S_kv keys (the cache already holds the new keys: q_offset + T_q <= S_kv).

@@ -182,3 +182,32 @@ def test_decode_empty_batch_is_a_no_op(L):
 ])
 def test_prefill_bad_args_return_codes_without_launch(L, args, code):
     assert api.gqa_attn_prefill_ex(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    # k_cache, v_cache, k_new, v_new, positions, B, H_kv, d, capacity, n_sink
+    ((0, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 8, 2), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 1, 64, 8, 2), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 8, 8), api.GQA_ERR_INVALID_ARG),   # no window
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 8, -1), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 0, 0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 96, 8, 2), api.GQA_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE + 8, FAKE, FAKE, 1, 1, 64, 8, 2), api.GQA_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 2), 0),                         # empty batch
+])
+def test_ring_append_bad_args_return_codes_without_launch(L, args, code):
+    assert api.gqa_attn_ring_append(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    # q, k, v, o, lse, seqlens, B, H_q, H_kv, d, capacity, n_sink, scale, num_splits
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, 2, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 8, 1, 64, 256, 256, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 8, 1, 64, 256, -1, 0.125, 0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 8, 1, 96, 256, 2, 0.125, 0), api.GQA_ERR_UNSUPPORTED),
+    ((FAKE + 2, FAKE, FAKE, FAKE, 0, FAKE, 1, 8, 1, 64, 256, 2, 0.125, 0),
+     api.GQA_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 8, 1, 64, 256, 2, 0.125, 0), 0),        # empty batch
+])
+def test_decode_ring_bad_args_return_codes_without_launch(L, args, code):
+    assert api.gqa_attn_decode_ring(*args, None) == code
