@@ -11,14 +11,17 @@ from .gqa_oracle import (  # noqa: F401
     TILE_ALL_PAST,
     TILE_PARTIAL,
     attention,
+    attention_q8,
     attention_ring,
     attention_rows,
     combine_partials,
+    dequantize_q8,
     finalize,
     init_running,
     lse_merge,
     online_softmax_sweep,
     prefill_tile_classes,
+    quantize_q8,
     ring_slot,
     ring_visible_tokens,
     ring_write,

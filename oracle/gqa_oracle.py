@@ -401,3 +401,49 @@ def attention_ring(q, k_stream, v_stream, *, scale: float, seqlens, capacity: in
             o, l_, _ = _softmax_attend(scores, Vr)
             O[b, h], lse[b, h] = o[0], l_[0]
     return O, lse
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV cache.
+#
+# Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §4 item 3:
+# optional INT4 / INT8 KV quantisation, recommended for contexts above 4 K.
+# The page fixes no scheme. Reading: symmetric, one fp32 scale per (row, KV
+# head, token) = max |x| / 127 over the token's d values, codes
+# rint(x / scale) (round half to even) in [-127, 127]; an all-zero token gets
+# scale 0 and codes 0. Both divisions are single fp32 IEEE divisions, so the
+# codes are a deterministic function of the bf16 input. Dequantised values
+# are code * scale, exact in fp64.
+# ---------------------------------------------------------------------------
+
+
+def quantize_q8(x):
+    """x: [..., d] (any real dtype; bf16 values widen exactly to fp32).
+    Returns (codes int8 [..., d], scales float32 [...])."""
+    xf = np.asarray(to_f64(x), dtype=np.float32)
+    amax = np.max(np.abs(xf), axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    nz = scale > 0
+    safe = np.where(nz, scale, np.float32(1.0)).astype(np.float32)
+    codes = np.rint(xf / safe[..., None]).astype(np.float32)
+    codes = np.clip(codes, -127, 127)
+    codes = np.where(nz[..., None], codes, 0)
+    return codes.astype(np.int8), scale
+
+
+def dequantize_q8(codes, scales):
+    """codes [..., d] int8, scales [...] -> fp64 values codes * scale."""
+    return np.asarray(codes, dtype=np.float64) * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def attention_q8(q, k_codes, k_scales, v_codes, v_scales, *, scale: float, seqlens=None):
+    """Decode attention over an INT8 cache, by its definition: the plain
+    decode definition applied to the dequantised K and V.
+
+    q: [B, H_q, d]; k_codes, v_codes: [B, H_kv, S, d] int8 (token-major, as
+    the tokens were produced); k_scales, v_scales: [B, H_kv, S].
+    Returns O [B, H_q, d], lse [B, H_q]."""
+    K = dequantize_q8(k_codes, k_scales)
+    V = dequantize_q8(v_codes, v_scales)
+    O, lse = attention(to_f64(q)[:, :, None, :], K, V, scale=scale, seqlens=seqlens)
+    return O[:, :, 0], lse[:, :, 0]
