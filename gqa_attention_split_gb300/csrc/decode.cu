@@ -78,21 +78,30 @@ struct SplitParams {
     int ring;                 // ring-buffer cache: a row longer than S_max keeps S_max slots
 };
 
-template <int D, int TILE_T, int STAGES, int WARPS>
+// Q8: the cache holds int8 codes, K token-major [S][D] and V dim-major
+// [D][S], with one fp32 scale per token for each (see gqa_attn_decode_q8).
+template <int D, int TILE_T, int STAGES, int WARPS, bool Q8 = false>
 struct SplitCfg {
     static constexpr int kThreads = WARPS * 32;
-    static constexpr int kBoxes = D / 64;               // 128-byte column boxes per row
-    static constexpr int kBoxBytes = TILE_T * 128;      // one box: TILE_T rows x 128 B
-    static constexpr int kKBytes = kBoxes * kBoxBytes;  // K (or V) part of a stage
-    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kBoxes = D / 64;               // bf16: 128-byte column boxes per row
+    static constexpr int kBoxBytes = TILE_T * 128;      // bf16: one box, TILE_T rows x 128 B
+    static constexpr int kKBytes = Q8 ? TILE_T * D : kBoxes * kBoxBytes;  // K part of a stage
+    static constexpr int kVBytes = Q8 ? D * TILE_T : kKBytes;             // V (or V^T) part
+    static constexpr int kStageBytes = kKBytes + kVBytes;
     static constexpr int kRingBytes = WARPS * STAGES * kStageBytes;
+    // Q8: per-token scales of K and V for every stage, [WARPS][STAGES][2][TILE_T]
+    static constexpr int kScaleOffset = kRingBytes;
+    static constexpr int kScaleBytes = Q8 ? WARPS * STAGES * 2 * TILE_T * 4 : 0;
+    static constexpr int kTxBytes = kStageBytes + (Q8 ? 2 * TILE_T * 4 : 0);  // per stage
     // Per-head record a CTA sends to the head's owner in the cluster:
     // {m, l, 0, 0, O[0..D)} as floats (16 + 4*D bytes, a multiple of 16).
     static constexpr int kRec = 4 + D;
     static constexpr int kRecBytes = kRec * 4;
     static constexpr int kWarpMergeFloats = (WARPS - 1) * (D / 16 * 4 + 4) * 32;
     static constexpr int kMergeBytes = kWarpMergeFloats * 4;
-    static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+    static constexpr int kDataBytes = kRingBytes + kScaleBytes > kMergeBytes
+                                          ? kRingBytes + kScaleBytes
+                                          : kMergeBytes;
     // Inbound records: [heads per rank][CS][kRec]. A rank owns ceil(8 / CS)
     // heads, so it receives at most 16 records for any CS <= 16.
     static constexpr int kRecvOffset = kDataBytes;
@@ -103,6 +112,8 @@ struct SplitCfg {
     static constexpr int kKC = D / 16;                  // 16-wide k-chunks of a head dim
     static_assert(TILE_T % 16 == 0 && TILE_T <= 256, "tile");
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(!Q8 || (D == 128 && TILE_T == 64), "int8 tiles: 64 tokens of a 128-dim head");
+    static_assert(kStageBytes % 1024 == 0, "stages stay aligned for the TMA swizzle");
 };
 
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -155,11 +166,13 @@ __device__ __forceinline__ void emit(const SplitParams& p, size_t row, int gi, i
     }
 }
 
-template <int D, int TILE_T, int STAGES, int WARPS, int CS>
+template <int D, int TILE_T, int STAGES, int WARPS, int CS, bool Q8>
 __global__ void __launch_bounds__(WARPS * 32, 1)
     split_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                 const __grid_constant__ CUtensorMap tmap_v, const SplitParams p) {
-    using C = SplitCfg<D, TILE_T, STAGES, WARPS>;
+                 const __grid_constant__ CUtensorMap tmap_v,
+                 const __grid_constant__ CUtensorMap tmap_ks,
+                 const __grid_constant__ CUtensorMap tmap_vs, const SplitParams p) {
+    using C = SplitCfg<D, TILE_T, STAGES, WARPS, Q8>;
     const int s = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
     const int gi = s / CS;         // cluster (group) index within the row
     const int rank = s % CS;       // == %cluster_ctarank for a (CS, 1, 1) cluster
@@ -193,6 +206,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
+        if constexpr (Q8) {
+            tma_prefetch_desc(&tmap_ks);
+            tma_prefetch_desc(&tmap_vs);
+        }
     }
     __syncwarp();
     // Cluster barrier, phase 0: every CTA of the cluster is running before any
@@ -208,15 +225,28 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         int hint = p.seqlens ? *reinterpret_cast<const volatile int32_t*>(p.seqlens + b) : p.S_max;
         hint = hint < 0 ? 0 : (hint > p.S_max ? p.S_max : hint);
         const SplitRange rh = split_range(p.L, s, hint);
-        const int nt = (rh.end - rh.start + TILE_T - 1) / TILE_T;
+        // bf16 tiles start at the split's first key; int8 tiles sit on
+        // TILE_T-aligned keys (see below)
+        const int hbase = Q8 ? rh.start - rh.start % TILE_T : rh.start;
+        const int nt = rh.end > rh.start ? (rh.end - hbase + TILE_T - 1) / TILE_T : 0;
         const int mine = warp < nt ? (nt - warp + WARPS - 1) / WARPS : 0;
-        constexpr int kPf = 2 * C::kBoxes;  // K and V boxes of one tile
+        constexpr int kPf = Q8 ? 4 : 2 * C::kBoxes;  // the copies of one tile
         static_assert(GQA_DEC_WARM_TILES * kPf <= 32, "one lane per prefetch");
         if (lane < min(GQA_DEC_WARM_TILES, mine) * kPf) {
             const int i = lane / kPf, j = lane % kPf;
-            const int tok0 = rh.start + (warp + i * WARPS) * TILE_T;
-            const int y = tok0 + TILE_T <= rh.end ? tok0 : rh.end - TILE_T;
-            tma_prefetch_l2_3d((j & 1) ? &tmap_v : &tmap_k, (j >> 1) * 64, y, b * p.H_kv + kv);
+            const int tok0 = hbase + (warp + i * WARPS) * TILE_T;
+            const int z = b * p.H_kv + kv;
+            if constexpr (Q8) {
+                if (j == 0)
+                    tma_prefetch_l2_3d(&tmap_k, 0, tok0, z);
+                else if (j == 1)
+                    tma_prefetch_l2_3d(&tmap_v, tok0, 0, z);
+                else
+                    tma_prefetch_l2_2d(j == 2 ? &tmap_ks : &tmap_vs, tok0, z);
+            } else {
+                const int y = tok0 + TILE_T <= rh.end ? tok0 : rh.end - TILE_T;
+                tma_prefetch_l2_3d((j & 1) ? &tmap_v : &tmap_k, (j >> 1) * 64, y, z);
+            }
         }
     }
 
@@ -239,7 +269,13 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     }
     const SplitRange r = s < p.ns ? split_range(p.L, s, seqlen) : SplitRange{seqlen, seqlen};
     const int len = r.end - r.start;
-    const int n_tiles = (len + TILE_T - 1) / TILE_T;
+    // bf16 tiles start at r.start (the last one shifted back to end at
+    // r.end, so only real rows load). int8 tiles sit on TILE_T-aligned keys
+    // (a TMA box of the dim-major V codes must start on a 16-byte boundary);
+    // keys of a tile outside [r.start, r.end) are masked, and padding codes are
+    // finite, so no P = 0 row can turn into NaN.
+    const int base = Q8 ? r.start - r.start % TILE_T : r.start;
+    const int n_tiles = len > 0 ? (r.end - base + TILE_T - 1) / TILE_T : 0;
     const int my_n = warp < n_tiles ? (n_tiles - warp + WARPS - 1) / WARPS : 0;
     const int zc = b * p.H_kv + kv;  // outer TMA coordinate: (batch, KV head)
 
@@ -249,19 +285,32 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         const int tok0 = r.start + (warp + i * WARPS) * TILE_T;
         return tok0 + TILE_T <= r.end ? tok0 : r.end - TILE_T;
     };
-    // A stage is 2 * kBoxes copies (K and V, 64 columns each). Lane 0 arms
-    // the stage's barrier, then each copy goes out from its own lane.
-    constexpr int kCopies = 2 * C::kBoxes;
+    float* scales = reinterpret_cast<float*>(smem + C::kScaleOffset);  // int8 only
+    // A bf16 stage is 2 * kBoxes copies (K and V, 64 columns each); an int8
+    // stage is K codes, V codes, K scales, V scales. Lane 0 arms the stage's
+    // barrier, then each copy goes out from its own lane.
+    constexpr int kCopies = Q8 ? 4 : 2 * C::kBoxes;
     static_assert(STAGES * kCopies <= 32, "one lane per copy of the first stages");
-    auto copy = [&](int i, int j) {  // copy j of tile i: K or V (j & 1), box j >> 1
+    auto copy = [&](int i, int j) {
         const int slot = i % STAGES;
-        const uint32_t dst = smem_u32(ring + slot * C::kStageBytes) + (j & 1) * C::kKBytes +
-                             (j >> 1) * C::kBoxBytes;
-        tma_load_3d(dst, (j & 1) ? &tmap_v : &tmap_k, (j >> 1) * 64, tile_y(i), zc,
-                    smem_u32(&bars[slot]), policy);
+        const uint32_t bar = smem_u32(&bars[slot]);
+        const uint32_t stage = smem_u32(ring + slot * C::kStageBytes);
+        if constexpr (Q8) {
+            const int t0 = base + (warp + i * WARPS) * TILE_T;
+            if (j == 0)
+                tma_load_3d(stage, &tmap_k, 0, t0, zc, bar, policy);
+            else if (j == 1)
+                tma_load_3d(stage + C::kKBytes, &tmap_v, t0, 0, zc, bar, policy);
+            else
+                tma_load_2d(smem_u32(scales + ((warp * STAGES + slot) * 2 + (j - 2)) * TILE_T),
+                            j == 2 ? &tmap_ks : &tmap_vs, t0, zc, bar, policy);
+        } else {  // K or V (j & 1), box j >> 1
+            tma_load_3d(stage + (j & 1) * C::kKBytes + (j >> 1) * C::kBoxBytes,
+                        (j & 1) ? &tmap_v : &tmap_k, (j >> 1) * 64, tile_y(i), zc, bar, policy);
+        }
     };
     auto issue = [&](int i) {  // the whole warp
-        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars[i % STAGES]), C::kStageBytes);
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars[i % STAGES]), C::kTxBytes);
         __syncwarp();
         if (lane < kCopies) copy(i, lane);
     };
@@ -272,21 +321,32 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     const int issued0 = min(STAGES, my_n);
     if (lane == 0)
         for (int i = withhold ? 1 : 0; i < issued0; ++i)
-            mbar_arrive_expect_tx(smem_u32(&bars[i]), C::kStageBytes);
+            mbar_arrive_expect_tx(smem_u32(&bars[i]), C::kTxBytes);
     __syncwarp();
     if (lane < issued0 * kCopies && !(withhold && lane < kCopies)) copy(lane / kCopies, lane % kCopies);
     int issued = issued0;
 
     // q^T as the B operand (k = head dim, n = query head g of this group).
+    // int8: f16 pairs, with the head dims in the order the K words are read
+    // (k step kc of lane c takes dims 32c + 4kc .. +3; see the S MMA below).
     uint32_t qf[C::kKC][2];
     {
         const bool has = g < p.G;
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            p.q + (size_t(b) * p.H_q + kv * p.G + (has ? g : 0)) * D);
+        const uint16_t* qh = p.q + (size_t(b) * p.H_q + kv * p.G + (has ? g : 0)) * D;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qh);
 #pragma unroll
         for (int kc = 0; kc < C::kKC; ++kc) {
-            qf[kc][0] = has ? qrow[(kc * 16 + 2 * c) / 2] : 0u;
-            qf[kc][1] = has ? qrow[(kc * 16 + 8 + 2 * c) / 2] : 0u;
+            if constexpr (Q8) {
+                const uint2 w = has ? *reinterpret_cast<const uint2*>(qh + 32 * c + 4 * kc)
+                                    : make_uint2(0u, 0u);
+                qf[kc][0] = pack_f16x2(__uint_as_float(w.x << 16),
+                                       __uint_as_float(w.x & 0xFFFF0000u));
+                qf[kc][1] = pack_f16x2(__uint_as_float(w.y << 16),
+                                       __uint_as_float(w.y & 0xFFFF0000u));
+            } else {
+                qf[kc][0] = has ? qrow[(kc * 16 + 2 * c) / 2] : 0u;
+                qf[kc][1] = has ? qrow[(kc * 16 + 8 + 2 * c) / 2] : 0u;
+            }
         }
     }
 
@@ -306,83 +366,205 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             if (alive) waited = i + 1;                // copies observed complete so far
         }
         if (i == 0 && threadIdx.x == 0) GQA_TRACE_STAMP(blin, 2);
-        const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
-        const uint32_t vbase = kbase + C::kKBytes;
-        const int tok0 = r.start + (warp + i * WARPS) * TILE_T;
-        const int y = tile_y(i);
-        const int lo = tok0, hi = min(tok0 + TILE_T, r.end);
+        if constexpr (!Q8) {
+            const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
+            const uint32_t vbase = kbase + C::kKBytes;
+            const int tok0 = r.start + (warp + i * WARPS) * TILE_T;
+            const int y = tile_y(i);
+            const int lo = tok0, hi = min(tok0 + TILE_T, r.end);
 
-        // ---- S^T = K_j q^T  (per 16-key m-tile, accumulate over the head dim)
-        float sc[C::kMT][4];
-#pragma unroll
-        for (int mt = 0; mt < C::kMT; ++mt) {
-            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-#pragma unroll
-            for (int kc = 0; kc < C::kKC; ++kc) {
-                const int mi = lane >> 3;
-                const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
-                const int ch = kc * 2 + (mi >> 1);
-                uint32_t a[4];
-                ldmatrix_x4(a, kbase + (ch >> 3) * C::kBoxBytes + swz128(row, ch & 7));
-                mma_bf16_16816(sc[mt], a, qf[kc][0], qf[kc][1]);
+            // ---- S^T = K_j q^T  (per 16-key m-tile, accumulate over the head dim)
+            float sc[C::kMT][4];
+    #pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+    #pragma unroll
+                for (int kc = 0; kc < C::kKC; ++kc) {
+                    const int mi = lane >> 3;
+                    const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                    const int ch = kc * 2 + (mi >> 1);
+                    uint32_t a[4];
+                    ldmatrix_x4(a, kbase + (ch >> 3) * C::kBoxBytes + swz128(row, ch & 7));
+                    mma_bf16_16816(sc[mt], a, qf[kc][0], qf[kc][1]);
+                }
             }
-        }
 
-        // ---- scale, mask (select), running max over keys for heads 2c, 2c+1
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < C::kMT; ++mt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int pos = y + mt * 16 + g + (e >> 1) * 8;
-                const bool ok = pos >= lo && pos < hi;
-                sc[mt][e] = ok ? sc[mt][e] * p.scale_log2 : -INFINITY;
+            // ---- scale, mask (select), running max over keys for heads 2c, 2c+1
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+    #pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int pos = y + mt * 16 + g + (e >> 1) * 8;
+                    const bool ok = pos >= lo && pos < hi;
+                    sc[mt][e] = ok ? sc[mt][e] * p.scale_log2 : -INFINITY;
+                }
+                mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
+                mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
             }
-            mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
-            mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
-        }
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: >= 1 key valid
-        const float corr0 = fast_exp2(m0 - mn0), corr1 = fast_exp2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int mt = 0; mt < C::kMT; ++mt) {
-            sc[mt][0] = fast_exp2(sc[mt][0] - mn0);
-            sc[mt][1] = fast_exp2(sc[mt][1] - mn1);
-            sc[mt][2] = fast_exp2(sc[mt][2] - mn0);
-            sc[mt][3] = fast_exp2(sc[mt][3] - mn1);
-            ps0 += sc[mt][0] + sc[mt][2];
-            ps1 += sc[mt][1] + sc[mt][3];
-        }
-        l0 = l0 * corr0 + ps0;
-        l1 = l1 * corr1 + ps1;
-#pragma unroll
-        for (int md = 0; md < C::kKC; ++md) {
-            acc[md][0] *= corr0;
-            acc[md][1] *= corr1;
-            acc[md][2] *= corr0;
-            acc[md][3] *= corr1;
-        }
+    #pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: >= 1 key valid
+            const float corr0 = fast_exp2(m0 - mn0), corr1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+    #pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                sc[mt][0] = fast_exp2(sc[mt][0] - mn0);
+                sc[mt][1] = fast_exp2(sc[mt][1] - mn1);
+                sc[mt][2] = fast_exp2(sc[mt][2] - mn0);
+                sc[mt][3] = fast_exp2(sc[mt][3] - mn1);
+                ps0 += sc[mt][0] + sc[mt][2];
+                ps1 += sc[mt][1] + sc[mt][3];
+            }
+            l0 = l0 * corr0 + ps0;
+            l1 = l1 * corr1 + ps1;
+    #pragma unroll
+            for (int md = 0; md < C::kKC; ++md) {
+                acc[md][0] *= corr0;
+                acc[md][1] *= corr1;
+                acc[md][2] *= corr0;
+                acc[md][3] *= corr1;
+            }
 
-        // ---- O^T += V_j^T P^T  (k = keys, 16 per step)
+            // ---- O^T += V_j^T P^T  (k = keys, 16 per step)
+    #pragma unroll
+            for (int kt = 0; kt < C::kMT; ++kt) {
+                const uint32_t b_lo = movmatrix_trans(pack_bf16x2(sc[kt][0], sc[kt][1]));
+                const uint32_t b_hi = movmatrix_trans(pack_bf16x2(sc[kt][2], sc[kt][3]));
+    #pragma unroll
+                for (int md = 0; md < C::kKC; ++md) {
+                    const int mi = lane >> 3;
+                    const int tok = kt * 16 + (mi >> 1) * 8 + (lane & 7);
+                    const int ch = md * 2 + (mi & 1);
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, vbase + (ch >> 3) * C::kBoxBytes + swz128(tok, ch & 7));
+                    mma_bf16_16816(acc[md], a, b_lo, b_hi);
+                }
+            }
+
+        } else {
+            // int8 codes: K rows are tokens [TILE_T][128 B] (128-byte swizzle),
+            // V rows are head dims [D][TILE_T B] (64-byte swizzle). Each 16-key
+            // m-tile of the MMAs takes its keys in the order pi(m) = 4(m&7 >> 1)
+            // + (m & 1) + 2(m >> 3), so that a lane's B-operand keys of the P.V
+            // step (logical 2c, 2c+1, 2c+8, 2c+9) are the four consecutive
+            // codes 4c .. 4c+3 of a V row: one 32-bit load. The sum over keys
+            // does not depend on their order. Scores and P are scaled per token
+            // after the MMAs (K) and before them (V).
+            const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
+            const uint32_t vbase = kbase + C::kKBytes;
+            const float* ksc = scales + (warp * STAGES + slot) * 2 * TILE_T;
+            const float* vsc = ksc + TILE_T;
+            const int tok0 = base + (warp + i * WARPS) * TILE_T;
+            const int lo = max(tok0, r.start), hi = min(tok0 + TILE_T, r.end);
+            const int kr0 = 4 * (g >> 1) + (g & 1);  // pi(g); pi(g + 8) = kr0 + 2
+
+            // ---- S^T = K_j q^T: lane c reads dims [32c, 32c + 32) of its two
+            // key rows (two 16-byte chunks each) and converts them to f16.
+            float sc[C::kMT][4];
+            bool ok[C::kMT][2];
 #pragma unroll
-        for (int kt = 0; kt < C::kMT; ++kt) {
-            const uint32_t b_lo = movmatrix_trans(pack_bf16x2(sc[kt][0], sc[kt][1]));
-            const uint32_t b_hi = movmatrix_trans(pack_bf16x2(sc[kt][2], sc[kt][3]));
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+                uint32_t w[2][8];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int row = mt * 16 + kr0 + 2 * rr;
+#pragma unroll
+                    for (int hc = 0; hc < 2; ++hc) {
+                        const uint4 v4 = ld_shared_v4(kbase + row * 128 +
+                                                      (((2 * c + hc) ^ (row & 7)) << 4));
+                        w[rr][hc * 4 + 0] = v4.x;
+                        w[rr][hc * 4 + 1] = v4.y;
+                        w[rr][hc * 4 + 2] = v4.z;
+                        w[rr][hc * 4 + 3] = v4.w;
+                    }
+                }
+#pragma unroll
+                for (int kc = 0; kc < C::kKC; ++kc) {
+                    uint32_t a[4];
+                    s8x4_to_f16x4(w[0][kc], a[0], a[2]);
+                    s8x4_to_f16x4(w[1][kc], a[1], a[3]);
+                    mma_f16_16816(sc[mt], a, qf[kc][0], qf[kc][1]);
+                }
+            }
+
+            // ---- scale by the token's K scale, mask (select), running max
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int key = mt * 16 + kr0 + 2 * rr;
+                    const int pos = tok0 + key;
+                    ok[mt][rr] = pos >= lo && pos < hi;
+                    const float f = ksc[key] * p.scale_log2;
+                    sc[mt][2 * rr] = ok[mt][rr] ? sc[mt][2 * rr] * f : -INFINITY;
+                    sc[mt][2 * rr + 1] = ok[mt][rr] ? sc[mt][2 * rr + 1] * f : -INFINITY;
+                }
+                mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
+                mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: >= 1 key valid
+            const float corr0 = fast_exp2(m0 - mn0), corr1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                sc[mt][0] = fast_exp2(sc[mt][0] - mn0);
+                sc[mt][1] = fast_exp2(sc[mt][1] - mn1);
+                sc[mt][2] = fast_exp2(sc[mt][2] - mn0);
+                sc[mt][3] = fast_exp2(sc[mt][3] - mn1);
+                ps0 += sc[mt][0] + sc[mt][2];
+                ps1 += sc[mt][1] + sc[mt][3];
+                // P times the token's V scale; a masked key gives exactly 0
+                // whatever scale its (padding) slot holds
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const float f = vsc[mt * 16 + kr0 + 2 * rr];
+                    sc[mt][2 * rr] = ok[mt][rr] ? sc[mt][2 * rr] * f : 0.f;
+                    sc[mt][2 * rr + 1] = ok[mt][rr] ? sc[mt][2 * rr + 1] * f : 0.f;
+                }
+            }
+            l0 = l0 * corr0 + ps0;
+            l1 = l1 * corr1 + ps1;
 #pragma unroll
             for (int md = 0; md < C::kKC; ++md) {
-                const int mi = lane >> 3;
-                const int tok = kt * 16 + (mi >> 1) * 8 + (lane & 7);
-                const int ch = md * 2 + (mi & 1);
-                uint32_t a[4];
-                ldmatrix_x4_trans(a, vbase + (ch >> 3) * C::kBoxBytes + swz128(tok, ch & 7));
-                mma_bf16_16816(acc[md], a, b_lo, b_hi);
+                acc[md][0] *= corr0;
+                acc[md][1] *= corr1;
+                acc[md][2] *= corr0;
+                acc[md][3] *= corr1;
+            }
+
+            // ---- O^T += V_j^T P^T: lane (g, c) reads codes 4c .. 4c+3 of the
+            // 16-key group kt for dims md*16 + g and + 8.
+#pragma unroll
+            for (int kt = 0; kt < C::kMT; ++kt) {
+                const uint32_t b_lo = movmatrix_trans(pack_f16x2(sc[kt][0], sc[kt][1]));
+                const uint32_t b_hi = movmatrix_trans(pack_f16x2(sc[kt][2], sc[kt][3]));
+#pragma unroll
+                for (int md = 0; md < C::kKC; ++md) {
+                    const int d0 = md * 16 + g, d1 = d0 + 8;
+                    const uint32_t w0 =
+                        ld_shared_u32(vbase + d0 * TILE_T + ((kt ^ ((d0 >> 1) & 3)) << 4) + 4 * c);
+                    const uint32_t w1 =
+                        ld_shared_u32(vbase + d1 * TILE_T + ((kt ^ ((d1 >> 1) & 3)) << 4) + 4 * c);
+                    uint32_t a[4];
+                    s8x4_to_f16x4(w0, a[0], a[2]);
+                    s8x4_to_f16x4(w1, a[1], a[3]);
+                    mma_f16_16816(acc[md], a, b_lo, b_hi);
+                }
             }
         }
 
@@ -645,6 +827,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #define GQA_DEC_WARPS 2
 #endif
 constexpr int kTileT = GQA_DEC_TILE_T, kStages = GQA_DEC_STAGES, kWarps = GQA_DEC_WARPS;
+constexpr int kTileTQ8 = 64;  // int8 caches: 64 tokens per stage (8 KB of K codes)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -672,11 +855,12 @@ WsLayout ws_layout(int B, int H_q, int d, int ns, int cs) {
     return w;
 }
 
-template <int D, int CS>
-int launch_split(const SplitParams& sp, const CUtensorMap& tk, const CUtensorMap& tv,
-                 cudaStream_t stream) {
-    using C = SplitCfg<D, kTileT, kStages, kWarps>;
-    auto kern = split_kernel<D, kTileT, kStages, kWarps, CS>;
+// maps: K, V (bf16) or K codes, V codes, K scales, V scales (int8).
+template <int D, int CS, bool Q8>
+int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream_t stream) {
+    constexpr int kT = Q8 ? kTileTQ8 : kTileT;
+    using C = SplitCfg<D, kT, kStages, kWarps, Q8>;
+    auto kern = split_kernel<D, kT, kStages, kWarps, CS, Q8>;
     static bool attr_set = false;  // benign race: setting it twice is harmless
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -707,20 +891,20 @@ int launch_split(const SplitParams& sp, const CUtensorMap& tk, const CUtensorMap
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CS > 1 ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, sp) != cudaSuccess) return GQA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], sp) != cudaSuccess)
+        return GQA_ERR_CUDA;
     return GQA_OK;
 }
 
-template <int D>
-int launch(const SplitParams& sp, int cs, const CUtensorMap& tk, const CUtensorMap& tv,
-           cudaStream_t stream) {
+template <int D, bool Q8>
+int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     int rc;
     switch (cs) {
-        case 16: rc = launch_split<D, 16>(sp, tk, tv, stream); break;
-        case 8: rc = launch_split<D, 8>(sp, tk, tv, stream); break;
-        case 4: rc = launch_split<D, 4>(sp, tk, tv, stream); break;
-        case 2: rc = launch_split<D, 2>(sp, tk, tv, stream); break;
-        default: rc = launch_split<D, 1>(sp, tk, tv, stream); break;
+        case 16: rc = launch_split<D, 16, Q8>(sp, maps, stream); break;
+        case 8: rc = launch_split<D, 8, Q8>(sp, maps, stream); break;
+        case 4: rc = launch_split<D, 4, Q8>(sp, maps, stream); break;
+        case 2: rc = launch_split<D, 2, Q8>(sp, maps, stream); break;
+        default: rc = launch_split<D, 1, Q8>(sp, maps, stream); break;
     }
     if (rc != GQA_OK || sp.n_groups == 1) return rc;
 
@@ -768,7 +952,9 @@ std::atomic<int> g_inject_timeout{0};
 
 int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse,
         const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max, float scale,
-        int ns, void* ws, size_t ws_bytes, cudaStream_t stream, bool ring = false) {
+        int ns, void* ws, size_t ws_bytes, cudaStream_t stream, bool ring = false,
+        const float* k_scales = nullptr, const float* v_scales = nullptr) {
+    const bool q8 = k_scales != nullptr;  // k, v are then int8 K codes and dim-major V codes
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
     const int cs = cluster_size_for(ns, int64_t(ns) * H_kv * B);
@@ -777,13 +963,33 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
         if (!ws || ws_bytes < wl.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
             return GQA_ERR_WORKSPACE;
     }
-    CUtensorMap tk, tv;
+    CUtensorMap maps[4];
     const uint64_t outer = uint64_t(B) * H_kv;
-    if (encode_tmap_3d_bf16(&tk, k, d, S_max, outer, 64, kTileT, CU_TENSOR_MAP_SWIZZLE_128B) !=
-            cudaSuccess ||
-        encode_tmap_3d_bf16(&tv, v, d, S_max, outer, 64, kTileT, CU_TENSOR_MAP_SWIZZLE_128B) !=
-            cudaSuccess)
-        return GQA_ERR_CUDA;
+    if (q8) {
+        const uint64_t kd[3] = {uint64_t(d), uint64_t(S_max), outer};  // K codes [.., S, d]
+        const uint32_t kb[3] = {uint32_t(d), kTileTQ8, 1};
+        const uint64_t vd[3] = {uint64_t(S_max), uint64_t(d), outer};  // V codes [.., d, S]
+        const uint32_t vb[3] = {kTileTQ8, uint32_t(d), 1};
+        const uint64_t sd[2] = {uint64_t(S_max), outer};                // scales [.., S]
+        const uint32_t sb[2] = {kTileTQ8, 1};
+        if (encode_tmap(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, k, kd, kb,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+            encode_tmap(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, v, vd, vb,
+                        CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess ||
+            encode_tmap(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, k_scales, sd, sb,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess ||
+            encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, v_scales, sd, sb,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    } else {
+        if (encode_tmap_3d_bf16(&maps[0], k, d, S_max, outer, 64, kTileT,
+                                CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+            encode_tmap_3d_bf16(&maps[1], v, d, S_max, outer, 64, kTileT,
+                                CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+            return GQA_ERR_CUDA;
+        maps[2] = maps[0];  // unused by the bf16 kernels
+        maps[3] = maps[1];
+    }
     SplitParams sp{};
     sp.q = q;
     sp.seqlens = seqlens;
@@ -817,7 +1023,9 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.trace_row0 = trace_row;
     trace_row += ns * H_kv * B;
 #endif
-    return d == 128 ? launch<128>(sp, cs, tk, tv, stream) : launch<64>(sp, cs, tk, tv, stream);
+    if (q8) return launch<128, true>(sp, cs, maps, stream);
+    return d == 128 ? launch<128, false>(sp, cs, maps, stream)
+                    : launch<64, false>(sp, cs, maps, stream);
 }
 
 }  // namespace decode
@@ -958,6 +1166,134 @@ extern "C" int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const 
                        stream, /*ring=*/true);
 }
 
+// ---------------------------------------------------------------------------
+// INT8 KV cache.
+//
+// Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §4 item 3
+// (optional INT4 / INT8 KV quantisation for long contexts; the page fixes no
+// scheme). Each (batch row, KV head, token) of K and of V gets one fp32 scale
+// max|x| / 127 and codes rint(x / scale) in [-127, 127] (ties to even; both
+// divisions single IEEE fp32 divisions; an all-zero token gets scale 0 and
+// codes 0). K codes stay token-major [S][d]; V codes are stored dim-major
+// [d][S] so that the decode kernel's P.V operand reads four consecutive
+// tokens of one dim with a single 32-bit load.
+
+namespace gqa {
+namespace decode {
+
+constexpr int kQuantTokens = 32;  // tokens per block; one warp per token at a time
+
+__global__ void __launch_bounds__(256)
+    quantize_kv_q8_kernel(const uint16_t* k, const uint16_t* v, int8_t* kc, int8_t* vc,
+                          float* ks, float* vs, int S) {
+    __shared__ uint32_t vt[128][kQuantTokens / 4];  // V codes of this block, dim-major
+    const int bh = blockIdx.y, t0 = blockIdx.x * kQuantTokens;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int tt = warp; tt < kQuantTokens; tt += 8) {
+        const int t = t0 + tt;
+        uint32_t vcode = 0;
+        if (t < S) {
+            const size_t row = size_t(bh) * S + t;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t* src = (which ? v : k) + row * 128;
+                const uint2 w = reinterpret_cast<const uint2*>(src)[lane];  // dims 4l .. 4l+3
+                float x[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                              __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u)};
+                float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+                amax = warp_max(amax);
+                const float sc = __fdiv_rn(amax, 127.f);
+                uint32_t packed = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float qv = sc > 0.f ? rintf(__fdiv_rn(x[e], sc)) : 0.f;
+                    qv = fminf(fmaxf(qv, -127.f), 127.f);
+                    packed |= (uint32_t(int(qv)) & 0xFFu) << (8 * e);
+                }
+                if (which == 0) {
+                    reinterpret_cast<uint32_t*>(kc + row * 128)[lane] = packed;
+                    if (lane == 0) ks[row] = sc;
+                } else {
+                    vcode = packed;
+                    if (lane == 0) vs[row] = sc;
+                }
+            }
+        }
+        // byte e of vcode is dim 4*lane + e of token tt
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            reinterpret_cast<uint8_t*>(&vt[4 * lane + e][0])[tt] = uint8_t(vcode >> (8 * e));
+    }
+    __syncthreads();
+    // dim-major rows: 32 consecutive tokens of one dim per 32-byte run
+    for (int i = threadIdx.x; i < 128 * (kQuantTokens / 4); i += blockDim.x) {
+        const int dim = i / (kQuantTokens / 4), wd = i % (kQuantTokens / 4);
+        const int t = t0 + 4 * wd;
+        int8_t* dst = vc + (size_t(bh) * 128 + dim) * S + t;
+        const uint32_t word = vt[dim][wd];
+        if (t + 3 < S) {
+            *reinterpret_cast<uint32_t*>(dst) = word;  // S % 16 == 0, t % 4 == 0: aligned
+        } else {
+            for (int e = 0; e < 4 && t + e < S; ++e) dst[e] = int8_t(word >> (8 * e));
+        }
+    }
+}
+
+}  // namespace decode
+}  // namespace gqa
+
+extern "C" int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, int8_t* k_codes,
+                                       int8_t* v_codes, float* k_scales, float* v_scales, int B,
+                                       int H_kv, int S, int d, cudaStream_t stream) {
+    if (!k || !v || !k_codes || !v_codes || !k_scales || !v_scales) return GQA_ERR_INVALID_ARG;
+    if (B < 0 || H_kv <= 0 || S <= 0) return GQA_ERR_INVALID_ARG;
+    if (d != 128 || S % 16 != 0) return GQA_ERR_UNSUPPORTED;
+    if (int64_t(B) * H_kv > 65535 || int64_t(B) * H_kv * S >= (int64_t(1) << 31))
+        return GQA_ERR_UNSUPPORTED;
+    for (const void* ptr : {static_cast<const void*>(k), static_cast<const void*>(v),
+                            static_cast<const void*>(k_codes), static_cast<const void*>(v_codes),
+                            static_cast<const void*>(k_scales), static_cast<const void*>(v_scales)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return GQA_ERR_MISALIGNED;
+    if (B == 0) return GQA_OK;
+    const dim3 grid(unsigned((S + decode::kQuantTokens - 1) / decode::kQuantTokens),
+                    unsigned(B * H_kv));
+    decode::quantize_kv_q8_kernel<<<grid, 256, 0, stream>>>(k, v, k_codes, v_codes, k_scales,
+                                                             v_scales, S);
+    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+extern "C" int gqa_attn_decode_q8(const uint16_t* q, const int8_t* k_codes,
+                                  const int8_t* v_codes, const float* k_scales,
+                                  const float* v_scales, uint16_t* o, float* lse,
+                                  const int32_t* seqlens, int B, int H_q, int H_kv, int d,
+                                  int S_max, float scale, int num_splits, cudaStream_t stream) {
+    if (!k_scales || !v_scales) return GQA_ERR_INVALID_ARG;
+    int rc = decode::check_args(q, k_codes, v_codes, o, B, H_q, H_kv, d, S_max, scale, num_splits);
+    if (rc != GQA_OK) return rc;
+    if (d != 128 || S_max % 16 != 0) return GQA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(k_scales) | reinterpret_cast<uintptr_t>(v_scales)) & 15u)
+        return GQA_ERR_MISALIGNED;
+    if (B == 0) return GQA_OK;
+    int ns = num_splits;
+    if (ns == 0) {
+        const int sms = num_sms();
+        if (sms <= 0) return GQA_ERR_CUDA;
+        ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
+        if (ns < 1) return GQA_ERR_INVALID_ARG;
+    }
+    const size_t bytes = decode::ws_layout(B, H_q, d, ns,
+                                           decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
+                             .total;
+    void* ws = nullptr;
+    if (bytes > 0) {
+        ws = stream_workspace(stream, bytes);
+        if (!ws) return GQA_ERR_WORKSPACE;
+    }
+    return decode::run(q, reinterpret_cast<const uint16_t*>(k_codes),
+                       reinterpret_cast<const uint16_t*>(v_codes), o, lse, seqlens, B, H_q, H_kv,
+                       d, S_max, scale, ns, ws, bytes, stream, /*ring=*/false, k_scales, v_scales);
+}
+
 #ifdef GQA_TRACE
 extern "C" int gqa_attn_trace_dump(void* host, size_t bytes, int clear) {
     if (bytes > sizeof(gqa::g_trace)) bytes = sizeof(gqa::g_trace);
@@ -1056,13 +1392,15 @@ extern "C" int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, con
 
     // The same launch sequence as gqa_attn_decode, with the fixed scratch and
     // status word in place of the library-owned ones.
-    CUtensorMap tk, tv;
+    CUtensorMap maps[4];
     const uint64_t outer = uint64_t(B) * H_kv;
-    if (gqa::encode_tmap_3d_bf16(&tk, k, d, S_max, outer, 64, kTileT,
+    if (gqa::encode_tmap_3d_bf16(&maps[0], k, d, S_max, outer, 64, kTileT,
                                  CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
-        gqa::encode_tmap_3d_bf16(&tv, v, d, S_max, outer, 64, kTileT,
+        gqa::encode_tmap_3d_bf16(&maps[1], v, d, S_max, outer, 64, kTileT,
                                  CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
         return GQA_ERR_CUDA;
+    maps[2] = maps[0];  // unused by the bf16 kernels
+    maps[3] = maps[1];
     SplitParams sp{};
     sp.q = q;
     sp.seqlens = seqlens;
@@ -1084,5 +1422,6 @@ extern "C" int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, con
     sp.n_groups = ns / cs;
     sp.warm_l2 = int64_t(ns) * H_kv * B <= num_sms() ? 1 : 0;  // a single wave
     sp.scale_log2 = scale * kLog2e;
-    return d == 128 ? launch<128>(sp, cs, tk, tv, stream) : launch<64>(sp, cs, tk, tv, stream);
+    return d == 128 ? launch<128, false>(sp, cs, maps, stream)
+                    : launch<64, false>(sp, cs, maps, stream);
 }

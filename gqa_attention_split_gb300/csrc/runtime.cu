@@ -85,9 +85,7 @@ void* stream_workspace(cudaStream_t stream, size_t bytes) {
     return p;
 }
 
-cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                                uint64_t outer, uint32_t box_inner, uint32_t box_rows,
-                                CUtensorMapSwizzle swizzle) {
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_encode) {
@@ -95,16 +93,44 @@ cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inn
             cudaDriverEntryPointQueryResult q;
             cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                                              cudaEnableDefault, &q);
-            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-                return e != cudaSuccess ? e : cudaErrorSymbolNotFound;
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return nullptr;
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
     }
+    return g_encode;
+}
+
+cudaError_t encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                        uint32_t rank, const void* base, const uint64_t* dims, const uint32_t* box,
+                        CUtensorMapSwizzle swizzle) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc || rank < 1 || rank > 5) return cudaErrorSymbolNotFound;
+    cuuint64_t d[5], strides[4];
+    cuuint32_t bx[5], estr[5];
+    uint64_t stride = elem_bytes;
+    for (uint32_t i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) strides[i - 1] = stride;
+        stride *= dims[i];
+    }
+    CUresult r = enc(map, dtype, rank, const_cast<void*>(base), d, strides, bx, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                                uint64_t outer, uint32_t box_inner, uint32_t box_rows,
+                                CUtensorMapSwizzle swizzle) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return cudaErrorSymbolNotFound;
     cuuint64_t dims[3] = {inner, rows, outer};
     cuuint64_t strides[2] = {inner * 2, inner * rows * 2};  // bytes, dims 1 and 2
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;

@@ -24,6 +24,11 @@ void* stream_workspace(cudaStream_t stream, size_t bytes);
 // Encodes a 3-D bf16 tensor map over a [outer, rows, inner] row-major tensor
 // with a {box_inner, box_rows, 1} box and the given swizzle. Returns
 // cudaSuccess or the error that describes the failure.
+// Tiled tensor map over a dense array: dims[0] is innermost, strides follow
+// from the dims (elem_bytes each).
+cudaError_t encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                        uint32_t rank, const void* base, const uint64_t* dims, const uint32_t* box,
+                        CUtensorMapSwizzle swizzle);
 cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner,
                                 uint64_t rows, uint64_t outer, uint32_t box_inner,
                                 uint32_t box_rows, CUtensorMapSwizzle swizzle);

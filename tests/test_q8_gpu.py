@@ -1,0 +1,142 @@
+"""GPU parity of the INT8 KV cache path.
+
+Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §4 item 3 (INT8
+KV quantisation; the scheme is the reading stated in the header and the
+oracle). The quantiser must reproduce the oracle's codes and scales bit for
+bit (integer work), and decode over a cache of the oracle's codes must match
+the oracle's attention over the dequantised cache within the decode
+tolerance: max |dO| <= 1e-2, mean |dO| <= 1e-3, |d lse| <= 1e-3.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from gqa_attention_split_gb300 import api, build
+from gqa_attention_split_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    api.lib()
+
+
+def _assert_close(o, lse, O_ref, L_ref, what):
+    o = o.float().cpu().double().numpy().reshape(O_ref.shape)
+    l = lse.cpu().double().numpy().reshape(L_ref.shape)
+    err = np.abs(o - O_ref)
+    assert np.isfinite(o).all(), what
+    assert err.max() <= MAX_ABS, f"{what} max|dO|={err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what} mean|dO|={err.mean():.3e}"
+    fin = np.isfinite(L_ref)
+    assert (np.isneginf(l) == ~fin).all(), what
+    if fin.any():
+        assert np.abs(l[fin] - L_ref[fin]).max() <= LSE_ABS, what
+
+
+def _oracle_cache(k, v):
+    """The oracle's codes and scales, in the kernel's layouts, on the GPU."""
+    kc, ks = orc.quantize_q8(k)
+    vc, vs = orc.quantize_q8(v)
+    dev = "cuda"
+    return (kc, ks, vc, vs,
+            torch.from_numpy(kc).to(dev), torch.from_numpy(np.ascontiguousarray(
+                np.swapaxes(vc, 2, 3))).to(dev),
+            torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev))
+
+
+def test_quantiser_matches_the_oracle_bit_for_bit():
+    B, H_kv, S, d = 2, 3, 96, 128
+    g = torch.Generator().manual_seed(41)
+    k = torch.randn(B, H_kv, S, d, generator=g).to(torch.bfloat16)
+    v = (3 * torch.randn(B, H_kv, S, d, generator=g)).to(torch.bfloat16)
+    # a token whose scale is exactly 1 and whose other values are ties
+    tie = torch.tensor([127.0] + [(-1) ** i * (i % 5 + 0.5) for i in range(d - 1)])
+    k[0, 0, 5] = tie.to(torch.bfloat16)
+    v[1, 2, 7] = (-tie).to(torch.bfloat16)
+    k[1, 1, 9] = 0   # all-zero tokens
+    v[0, 1, 95] = 0
+    kc, vc, ks, vs = api.quantize_kv_q8(k.cuda(), v.cuda())
+    api.check()
+    okc, oks = orc.quantize_q8(k)
+    ovc, ovs = orc.quantize_q8(v)
+    assert np.array_equal(kc.cpu().numpy(), okc)
+    assert np.array_equal(vc.cpu().numpy(), np.swapaxes(ovc, 2, 3))
+    assert np.array_equal(ks.cpu().numpy(), oks)
+    assert np.array_equal(vs.cpu().numpy(), ovs)
+    assert oks[0, 0, 5] == 1.0 and okc[0, 0, 5, 1] == 0  # rint(0.5) = 0
+
+
+@pytest.mark.parametrize("S_max,G", [(1024, 8), (3008, 4), (160, 1)])
+def test_decode_matches_the_oracle_on_ragged_rows(S_max, G):
+    lens = sorted({0, 1, 15, 16, 17, 63, 64, 65, min(100, S_max), S_max // 2 + 3, S_max})
+    B, H_kv, d = len(lens), 2, 128
+    q, k, v, _ = wl.small_decode(B, G * H_kv, H_kv, d, S_max, seed=900 + S_max + G)
+    kc, ks, vc, vs, dkc, dvc, dks, dvs = _oracle_cache(k, v)
+    # padding beyond each row's length: garbage codes and NaN scales must not leak
+    for b, n in enumerate(lens):
+        dkc[b, :, n:] = 77
+        dvc[b, :, :, n:] = -91
+        dks[b, :, n:] = float("nan")
+        dvs[b, :, n:] = float("nan")
+    sl = torch.tensor(lens, dtype=torch.int32)
+    O, L = orc.attention_q8(q, kc, ks, vc, vs, scale=1 / math.sqrt(d), seqlens=lens)
+    for ns in (0, 1, 2, 3, 16, 32):
+        o, lse = api.decode_q8(q.cuda(), dkc, dvc, dks, dvs, sl.cuda(), num_splits=ns)
+        api.check()
+        _assert_close(o, lse, O, L, f"S={S_max} G={G} ns={ns}")
+
+
+def test_full_size_8k_decode_through_the_gpu_quantiser():
+    w = wl.LLAMA70B_DECODE_8K
+    q, k, v, sl = wl.decode_inputs(w)
+    kc, vc, ks, vs = api.quantize_kv_q8(k.cuda(), v.cuda())
+    o, lse = api.decode_q8(q.cuda(), kc, vc, ks, vs, sl.cuda())
+    api.check()
+    okc, oks = orc.quantize_q8(k)
+    ovc, ovs = orc.quantize_q8(v)
+    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(ks.cpu().numpy(), oks)
+    O, L = orc.attention_q8(q, okc, oks, ovc, ovs, scale=w.scale, seqlens=sl.tolist())
+    _assert_close(o, lse, O, L, "8K")
+    # the quantised cache stays close to the bf16 one (information only: the
+    # parity bar above is against the dequantised cache)
+    O16, _ = orc.attention(q[:, :, None], k, v, scale=w.scale, seqlens=sl.tolist())
+    assert np.abs(O - O16[:, :, 0]).max() < 0.05
+
+
+def test_ragged_128k_sampled_heads():
+    w = wl.RAGGED_DECODE_128K
+    q, k, v, sl = wl.decode_inputs(w)
+    kc, vc, ks, vs = api.quantize_kv_q8(k.cuda(), v.cuda())
+    o, lse = api.decode_q8(q.cuda(), kc, vc, ks, vs, sl.cuda())
+    api.check()
+    o, lse = o.cpu(), lse.cpu()
+    G = w.H_q // w.H_kv
+    rng = np.random.default_rng(5)
+    for b in range(w.B):
+        for h in rng.choice(w.H_q, size=3, replace=False):
+            kv = h // G
+            n = int(sl[b])
+            kcb, ksb = orc.quantize_q8(k[b:b + 1, kv:kv + 1, :n])
+            vcb, vsb = orc.quantize_q8(v[b:b + 1, kv:kv + 1, :n])
+            O, L = orc.attention_q8(q[b:b + 1, h:h + 1], kcb, ksb, vcb, vsb, scale=w.scale)
+            _assert_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O, L, f"b={b} h={h}")
+
+
+def test_decode_rejects_unsupported_shapes():
+    q = torch.zeros(1, 8, 64, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(1, 1, 64, 64, dtype=torch.int8, device="cuda")
+    sc = torch.zeros(1, 1, 64, device="cuda")
+    with pytest.raises(api.GqaError) as e:
+        api.decode_q8(q, kc, kc.clone(), sc, sc.clone())
+    assert e.value.code == api.GQA_ERR_UNSUPPORTED
