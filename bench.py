@@ -516,7 +516,49 @@ def run_case(args):
     api.lib()
     dev = torch.device("cuda", 0)
     graph_call = None  # decode cases: the same call in a CUDA graph over rotating caches
-    if args.case in ("decode8k", "ragged128k", "ring8k"):
+    extra = None
+    if args.case in ("decode8k_q8", "ragged128k_q8"):
+        # INT8 cache: bytes read are the codes plus one fp32 scale per token for
+        # K and for V; the rate is also given as the bf16 bytes it replaces
+        w = wl.RAGGED_DECODE_128K if args.case == "ragged128k_q8" else wl.LLAMA70B_DECODE_8K
+        q, k, v, sl = (t.to(dev) for t in wl.decode_inputs(w))
+        caches = [api.quantize_kv_q8(k, v)]
+        del k, v
+        tokens = sum(min(int(x), w.S_max) for x in sl.tolist())
+        q8_bytes = tokens * w.H_kv * (2 * w.d + 8)
+        bf16_bytes = tokens * w.H_kv * 2 * w.d * 2
+        per_set = sum(t.numel() * t.element_size() for t in caches[0])
+        for _ in range(max(1, -(-300_000_000 // per_set)) - 1):
+            kk = torch.randn(w.B, w.H_kv, w.S_max, w.d, device=dev).to(torch.bfloat16)
+            vv = torch.randn(w.B, w.H_kv, w.S_max, w.d, device=dev).to(torch.bfloat16)
+            caches.append(api.quantize_kv_q8(kk, vv))
+            del kk, vv
+        torch.cuda.synchronize()
+        api.check()
+
+        def one(cset):
+            api.decode_q8(q, *cset, sl, num_splits=args.num_splits)
+
+        def call():
+            one(caches[0])
+
+        gs = torch.cuda.Stream()
+        with torch.cuda.stream(gs):
+            for cset in caches:
+                one(cset)
+        gs.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for cset in caches:
+                one(cset)
+
+        def graph_call():
+            graph.replay()
+
+        graph_calls = len(caches)
+        work, unit = q8_bytes / 1e9, "GB/s"
+        extra = {"int8_bytes_per_call": q8_bytes, "bf16_equivalent_bytes_per_call": bf16_bytes}
+    elif args.case in ("decode8k", "ragged128k", "ring8k"):
         w = wl.RAGGED_DECODE_128K if args.case == "ragged128k" else wl.LLAMA70B_DECODE_8K
         q, k, v, sl = (t.to(dev) for t in wl.decode_inputs(w))
         ring = args.case == "ring8k"
@@ -597,6 +639,9 @@ def run_case(args):
         res["graph"] = {"us_per_call": gmed * 1e6, "value": work / gmed, "calls_per_graph":
                         graph_calls, "note": "back-to-back calls in a CUDA graph over distinct "
                         "caches larger than L2 together"}
+        if extra:
+            res["graph"]["bf16_equivalent_GBps"] = extra["bf16_equivalent_bytes_per_call"] / gmed / 1e9
+            res.update(extra)
     print(json.dumps(res))
 
 

@@ -269,8 +269,8 @@ def gqa_attn_decode_q8(q, k_codes, v_codes, k_scales, v_scales, o, lse, seqlens,
 
 def quantize_kv_q8(k, v, *, stream=None):
     """INT8 cache from a bf16 cache k, v [B,H_kv,S,d] (CUDA): returns
-    (k_codes [B,H_kv,S,d] int8, v_codes [B,H_kv,d,S] int8, k_scales, v_scales
-    [B,H_kv,S] fp32)."""
+    (k_codes [B,H_kv,S,d], v_codes [B,H_kv,d,S] as uint8 bytes code + 128,
+    k_scales, v_scales [B,H_kv,S] fp32)."""
     import torch
 
     _check_cuda_bf16("k", k, 4)
@@ -278,8 +278,8 @@ def quantize_kv_q8(k, v, *, stream=None):
     if k.shape != v.shape:
         raise ValueError("k and v must have the same shape")
     B, H_kv, S, d = k.shape
-    kc = torch.empty((B, H_kv, S, d), dtype=torch.int8, device=k.device)
-    vc = torch.empty((B, H_kv, d, S), dtype=torch.int8, device=k.device)
+    kc = torch.empty((B, H_kv, S, d), dtype=torch.uint8, device=k.device)
+    vc = torch.empty((B, H_kv, d, S), dtype=torch.uint8, device=k.device)
     ks = torch.empty((B, H_kv, S), dtype=torch.float32, device=k.device)
     vs = torch.empty_like(ks)
     rc = gqa_attn_quantize_kv_q8(_ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), B, H_kv,
@@ -298,9 +298,9 @@ def decode_q8(q, k_codes, v_codes, k_scales, v_scales, seqlens=None, *, num_spli
     _check_cuda_bf16("q", q, 3)
     B, H_q, d = q.shape
     H_kv, S_max = k_codes.shape[1], k_codes.shape[2]
-    if (k_codes.dtype != torch.int8 or v_codes.dtype != torch.int8
+    if (k_codes.dtype != torch.uint8 or v_codes.dtype != torch.uint8
             or k_codes.shape != (B, H_kv, S_max, d) or v_codes.shape != (B, H_kv, d, S_max)):
-        raise ValueError("k_codes [B,H_kv,S,d] and v_codes [B,H_kv,d,S] must be int8")
+        raise ValueError("k_codes [B,H_kv,S,d] and v_codes [B,H_kv,d,S] must be uint8")
     for nm, t in (("k_scales", k_scales), ("v_scales", v_scales)):
         if t.dtype != torch.float32 or t.shape != (B, H_kv, S_max) or not t.is_contiguous():
             raise ValueError(f"{nm} must be a contiguous fp32 [B, H_kv, S] tensor")

@@ -112,7 +112,8 @@ struct SplitCfg {
     static constexpr int kKC = D / 16;                  // 16-wide k-chunks of a head dim
     static_assert(TILE_T % 16 == 0 && TILE_T <= 256, "tile");
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(!Q8 || (D == 128 && TILE_T == 64), "int8 tiles: 64 tokens of a 128-dim head");
+    static_assert(!Q8 || (D == 128 && (TILE_T == 32 || TILE_T == 64 || TILE_T == 128)),
+                  "int8 tiles: 32, 64 or 128 tokens of a 128-dim head");
     static_assert(kStageBytes % 1024 == 0, "stages stay aligned for the TMA swizzle");
 };
 
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // int8: f16 pairs, with the head dims in the order the K words are read
     // (k step kc of lane c takes dims 32c + 4kc .. +3; see the S MMA below).
     uint32_t qf[C::kKC][2];
+    float qsum = 0.f;  // int8: this lane's share of sum_d q[g][d] (f16 values)
     {
         const bool has = g < p.G;
         const uint16_t* qh = p.q + (size_t(b) * p.H_q + kv * p.G + (has ? g : 0)) * D;
@@ -343,6 +345,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                                        __uint_as_float(w.x & 0xFFFF0000u));
                 qf[kc][1] = pack_f16x2(__uint_as_float(w.y << 16),
                                        __uint_as_float(w.y & 0xFFFF0000u));
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][0]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][1]));
+                qsum += (f0.x + f0.y) + (f1.x + f1.y);
             } else {
                 qf[kc][0] = has ? qrow[(kc * 16 + 2 * c) / 2] : 0u;
                 qf[kc][1] = has ? qrow[(kc * 16 + 8 + 2 * c) / 2] : 0u;
@@ -350,6 +355,17 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
     }
 
+    // int8: the f16 codes are code + 1152, so the S MMA adds 1152 * sum_d q[h][d]
+    // to head h's scores (qoff, taken off before scaling) and the P.V MMA adds
+    // 1152 * sum_k P'[h][k] to every dim of head h (poff, this lane's share of
+    // the running sum of the f16 P' it fed the MMA; taken off at the end).
+    float qoff0 = 0.f, qoff1 = 0.f, poff0 = 0.f, poff1 = 0.f;
+    if constexpr (Q8) {
+        qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+        qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // lanes 4g .. 4g+3: head g
+        qoff0 = kQ8Offset * __shfl_sync(0xffffffffu, qsum, 8 * c);
+        qoff1 = kQ8Offset * __shfl_sync(0xffffffffu, qsum, 8 * c + 4);
+    }
     float m0 = -INFINITY, m1 = -INFINITY;  // heads 2c, 2c+1 (base-2 domain)
     float l0 = 0.f, l1 = 0.f;               // this lane's share of the row sums
     float acc[C::kKC][4];                   // O^T: rows = dims, cols = heads
@@ -488,8 +504,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 #pragma unroll
                 for (int kc = 0; kc < C::kKC; ++kc) {
                     uint32_t a[4];
-                    s8x4_to_f16x4(w[0][kc], a[0], a[2]);
-                    s8x4_to_f16x4(w[1][kc], a[1], a[3]);
+                    u8x4_to_f16x4_biased(w[0][kc], a[0], a[2]);
+                    u8x4_to_f16x4_biased(w[1][kc], a[1], a[3]);
                     mma_f16_16816(sc[mt], a, qf[kc][0], qf[kc][1]);
                 }
             }
@@ -504,8 +520,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                     const int pos = tok0 + key;
                     ok[mt][rr] = pos >= lo && pos < hi;
                     const float f = ksc[key] * p.scale_log2;
-                    sc[mt][2 * rr] = ok[mt][rr] ? sc[mt][2 * rr] * f : -INFINITY;
-                    sc[mt][2 * rr + 1] = ok[mt][rr] ? sc[mt][2 * rr + 1] * f : -INFINITY;
+                    sc[mt][2 * rr] =
+                        ok[mt][rr] ? (sc[mt][2 * rr] - qoff0) * f : -INFINITY;
+                    sc[mt][2 * rr + 1] =
+                        ok[mt][rr] ? (sc[mt][2 * rr + 1] - qoff1) * f : -INFINITY;
                 }
                 mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
                 mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
@@ -546,23 +564,41 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 acc[md][2] *= corr0;
                 acc[md][3] *= corr1;
             }
+            // P' as the MMA will see it (f16), and its per-head sums: the V
+            // codes carry the 1152 offset, removed once at the end
+            uint32_t pp[C::kMT][2];
+            float pv0 = 0.f, pv1 = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                pp[mt][0] = pack_f16x2(sc[mt][0], sc[mt][1]);
+                pp[mt][1] = pack_f16x2(sc[mt][2], sc[mt][3]);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pp[mt][0]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pp[mt][1]));
+                pv0 += f0.x + f1.x;
+                pv1 += f0.y + f1.y;
+            }
+            poff0 = poff0 * corr0 + pv0;
+            poff1 = poff1 * corr1 + pv1;
 
             // ---- O^T += V_j^T P^T: lane (g, c) reads codes 4c .. 4c+3 of the
             // 16-key group kt for dims md*16 + g and + 8.
 #pragma unroll
             for (int kt = 0; kt < C::kMT; ++kt) {
-                const uint32_t b_lo = movmatrix_trans(pack_f16x2(sc[kt][0], sc[kt][1]));
-                const uint32_t b_hi = movmatrix_trans(pack_f16x2(sc[kt][2], sc[kt][3]));
+                const uint32_t b_lo = movmatrix_trans(pp[kt][0]);
+                const uint32_t b_hi = movmatrix_trans(pp[kt][1]);
 #pragma unroll
                 for (int md = 0; md < C::kKC; ++md) {
                     const int d0 = md * 16 + g, d1 = d0 + 8;
-                    const uint32_t w0 =
-                        ld_shared_u32(vbase + d0 * TILE_T + ((kt ^ ((d0 >> 1) & 3)) << 4) + 4 * c);
-                    const uint32_t w1 =
-                        ld_shared_u32(vbase + d1 * TILE_T + ((kt ^ ((d1 >> 1) & 3)) << 4) + 4 * c);
+                    // the TMA swizzle of TILE_T-byte rows: the 16-byte chunk index
+                    // XOR bits 7.. of the row's byte offset
+                    constexpr int kChunkMask = TILE_T / 16 - 1;
+                    const uint32_t w0 = ld_shared_u32(
+                        vbase + d0 * TILE_T + ((kt ^ ((d0 * TILE_T >> 7) & kChunkMask)) << 4) + 4 * c);
+                    const uint32_t w1 = ld_shared_u32(
+                        vbase + d1 * TILE_T + ((kt ^ ((d1 * TILE_T >> 7) & kChunkMask)) << 4) + 4 * c);
                     uint32_t a[4];
-                    s8x4_to_f16x4(w0, a[0], a[2]);
-                    s8x4_to_f16x4(w1, a[1], a[3]);
+                    u8x4_to_f16x4_biased(w0, a[0], a[2]);
+                    u8x4_to_f16x4_biased(w1, a[1], a[3]);
                     mma_f16_16816(acc[md], a, b_lo, b_hi);
                 }
             }
@@ -583,6 +619,20 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if constexpr (Q8) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            poff0 += __shfl_xor_sync(0xffffffffu, poff0, off);
+            poff1 += __shfl_xor_sync(0xffffffffu, poff1, off);
+        }
+#pragma unroll
+        for (int md = 0; md < C::kKC; ++md) {
+            acc[md][0] -= kQ8Offset * poff0;
+            acc[md][1] -= kQ8Offset * poff1;
+            acc[md][2] -= kQ8Offset * poff0;
+            acc[md][3] -= kQ8Offset * poff1;
+        }
     }
     if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 3);
     // This CTA's K/V stream is done: the next kernel in the stream may launch
@@ -827,7 +877,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #define GQA_DEC_WARPS 2
 #endif
 constexpr int kTileT = GQA_DEC_TILE_T, kStages = GQA_DEC_STAGES, kWarps = GQA_DEC_WARPS;
-constexpr int kTileTQ8 = 64;  // int8 caches: 64 tokens per stage (8 KB of K codes)
+// int8 caches: 64 tokens per stage; a grid of one wave runs 2 warps x 3
+// stages per CTA, a longer grid 3 warps x 2 stages (GB300, 8K decode: 9.4 vs
+// 9.8 us; ragged 128K batch: 106 vs 97 us).
+constexpr int kTileTQ8 = 64;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -856,11 +909,11 @@ WsLayout ws_layout(int B, int H_q, int d, int ns, int cs) {
 }
 
 // maps: K, V (bf16) or K codes, V codes, K scales, V scales (int8).
-template <int D, int CS, bool Q8>
+template <int D, int CS, bool Q8, int kW = kWarps, int kS = kStages>
 int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     constexpr int kT = Q8 ? kTileTQ8 : kTileT;
-    using C = SplitCfg<D, kT, kStages, kWarps, Q8>;
-    auto kern = split_kernel<D, kT, kStages, kWarps, CS, Q8>;
+    using C = SplitCfg<D, kT, kS, kW, Q8>;
+    auto kern = split_kernel<D, kT, kS, kW, CS, Q8>;
     static bool attr_set = false;  // benign race: setting it twice is harmless
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -896,16 +949,25 @@ int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream
     return GQA_OK;
 }
 
+template <int D, bool Q8, int kW, int kS>
+int launch_cs(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
+    switch (cs) {
+        case 16: return launch_split<D, 16, Q8, kW, kS>(sp, maps, stream);
+        case 8: return launch_split<D, 8, Q8, kW, kS>(sp, maps, stream);
+        case 4: return launch_split<D, 4, Q8, kW, kS>(sp, maps, stream);
+        case 2: return launch_split<D, 2, Q8, kW, kS>(sp, maps, stream);
+        default: return launch_split<D, 1, Q8, kW, kS>(sp, maps, stream);
+    }
+}
+
 template <int D, bool Q8>
 int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     int rc;
-    switch (cs) {
-        case 16: rc = launch_split<D, 16, Q8>(sp, maps, stream); break;
-        case 8: rc = launch_split<D, 8, Q8>(sp, maps, stream); break;
-        case 4: rc = launch_split<D, 4, Q8>(sp, maps, stream); break;
-        case 2: rc = launch_split<D, 2, Q8>(sp, maps, stream); break;
-        default: rc = launch_split<D, 1, Q8>(sp, maps, stream); break;
-    }
+    if constexpr (Q8)
+        rc = sp.warm_l2 ? launch_cs<D, true, 2, 3>(sp, cs, maps, stream)
+                        : launch_cs<D, true, 3, 2>(sp, cs, maps, stream);
+    else
+        rc = launch_cs<D, false, kWarps, kStages>(sp, cs, maps, stream);
     if (rc != GQA_OK || sp.n_groups == 1) return rc;
 
     static bool attr_set = false;
@@ -975,7 +1037,9 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
         if (encode_tmap(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, k, kd, kb,
                         CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
             encode_tmap(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, v, vd, vb,
-                        CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess ||
+                        kTileTQ8 == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
+                        : kTileTQ8 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                         : CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
             encode_tmap(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, k_scales, sd, sb,
                         CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess ||
             encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, v_scales, sd, sb,
@@ -1174,7 +1238,8 @@ extern "C" int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const 
 // scheme). Each (batch row, KV head, token) of K and of V gets one fp32 scale
 // max|x| / 127 and codes rint(x / scale) in [-127, 127] (ties to even; both
 // divisions single IEEE fp32 divisions; an all-zero token gets scale 0 and
-// codes 0). K codes stay token-major [S][d]; V codes are stored dim-major
+// codes 0), stored biased as the bytes code + 128. K codes stay token-major
+// [S][d]; V codes are stored dim-major
 // [d][S] so that the decode kernel's P.V operand reads four consecutive
 // tokens of one dim with a single 32-bit load.
 
@@ -1184,7 +1249,7 @@ namespace decode {
 constexpr int kQuantTokens = 32;  // tokens per block; one warp per token at a time
 
 __global__ void __launch_bounds__(256)
-    quantize_kv_q8_kernel(const uint16_t* k, const uint16_t* v, int8_t* kc, int8_t* vc,
+    quantize_kv_q8_kernel(const uint16_t* k, const uint16_t* v, uint8_t* kc, uint8_t* vc,
                           float* ks, float* vs, int S) {
     __shared__ uint32_t vt[128][kQuantTokens / 4];  // V codes of this block, dim-major
     const int bh = blockIdx.y, t0 = blockIdx.x * kQuantTokens;
@@ -1208,7 +1273,7 @@ __global__ void __launch_bounds__(256)
                 for (int e = 0; e < 4; ++e) {
                     float qv = sc > 0.f ? rintf(__fdiv_rn(x[e], sc)) : 0.f;
                     qv = fminf(fmaxf(qv, -127.f), 127.f);
-                    packed |= (uint32_t(int(qv)) & 0xFFu) << (8 * e);
+                    packed |= uint32_t(int(qv) + 128) << (8 * e);  // stored biased
                 }
                 if (which == 0) {
                     reinterpret_cast<uint32_t*>(kc + row * 128)[lane] = packed;
@@ -1229,12 +1294,12 @@ __global__ void __launch_bounds__(256)
     for (int i = threadIdx.x; i < 128 * (kQuantTokens / 4); i += blockDim.x) {
         const int dim = i / (kQuantTokens / 4), wd = i % (kQuantTokens / 4);
         const int t = t0 + 4 * wd;
-        int8_t* dst = vc + (size_t(bh) * 128 + dim) * S + t;
+        uint8_t* dst = vc + (size_t(bh) * 128 + dim) * S + t;
         const uint32_t word = vt[dim][wd];
         if (t + 3 < S) {
             *reinterpret_cast<uint32_t*>(dst) = word;  // S % 16 == 0, t % 4 == 0: aligned
         } else {
-            for (int e = 0; e < 4 && t + e < S; ++e) dst[e] = int8_t(word >> (8 * e));
+            for (int e = 0; e < 4 && t + e < S; ++e) dst[e] = uint8_t(word >> (8 * e));
         }
     }
 }
@@ -1242,8 +1307,8 @@ __global__ void __launch_bounds__(256)
 }  // namespace decode
 }  // namespace gqa
 
-extern "C" int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, int8_t* k_codes,
-                                       int8_t* v_codes, float* k_scales, float* v_scales, int B,
+extern "C" int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
+                                       uint8_t* v_codes, float* k_scales, float* v_scales, int B,
                                        int H_kv, int S, int d, cudaStream_t stream) {
     if (!k || !v || !k_codes || !v_codes || !k_scales || !v_scales) return GQA_ERR_INVALID_ARG;
     if (B < 0 || H_kv <= 0 || S <= 0) return GQA_ERR_INVALID_ARG;
@@ -1262,8 +1327,8 @@ extern "C" int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, int
     return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-extern "C" int gqa_attn_decode_q8(const uint16_t* q, const int8_t* k_codes,
-                                  const int8_t* v_codes, const float* k_scales,
+extern "C" int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes,
+                                  const uint8_t* v_codes, const float* k_scales,
                                   const float* v_scales, uint16_t* o, float* lse,
                                   const int32_t* seqlens, int B, int H_q, int H_kv, int d,
                                   int S_max, float scale, int num_splits, cudaStream_t stream) {

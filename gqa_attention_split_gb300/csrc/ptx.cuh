@@ -263,17 +263,16 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Four int8 codes (bytes 0..3 of w) to two f16 pairs, exactly: each byte,
-// offset to x + 128, becomes the low mantissa byte of the f16 1024 + (x + 128)
-// (exponent byte 0x64), and subtracting 1152 leaves x. lo = (x0, x1),
-// hi = (x2, x3), the lower code in the low half.
-__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+// Four biased int8 codes (bytes u = x + 128 of w) to two f16 pairs: each
+// byte becomes the low mantissa byte of an f16 with exponent byte 0x64, i.e.
+// the exact value 1024 + u = 1152 + x. lo = bytes 0, 1; hi = bytes 2, 3 (the
+// lower byte in the low half). The caller removes the 1152 offset after the
+// MMA, where it is one product per head instead of one subtraction per code.
+__device__ __forceinline__ void u8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    lo = __byte_perm(w, 0x64646464u, 0x4140);
+    hi = __byte_perm(w, 0x64646464u, 0x4342);
 }
+constexpr float kQ8Offset = 1152.f;  // f16 value of a biased code minus the code
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;

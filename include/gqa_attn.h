@@ -173,27 +173,29 @@ int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const uint16_t* v
  * fixes no scheme). Here: one fp32 scale per (batch row, KV head, token) for K
  * and one for V, scale = max|x| / 127 over the token's d values, codes
  * rint(x / scale) in [-127, 127] (ties to even; both divisions are single IEEE
- * fp32 divisions; an all-zero token has scale 0 and codes 0). Layouts:
- *   k_codes  int8  [B, H_kv, S, d]   token-major, like the bf16 K cache
- *   v_codes  int8  [B, H_kv, d, S]   dim-major (V transposed)
+ * fp32 divisions; an all-zero token has scale 0 and codes 0). A code x is
+ * stored as the byte x + 128 (uint8, so 128 is zero). Layouts:
+ *   k_codes  uint8 [B, H_kv, S, d]   token-major, like the bf16 K cache
+ *   v_codes  uint8 [B, H_kv, d, S]   dim-major (V transposed)
  *   k_scales, v_scales  fp32 [B, H_kv, S]
  * d must be 128 and S a multiple of 16; every pointer 16-byte aligned. */
 
 /* Quantises a bf16 cache k, v [B, H_kv, S, d] into the layouts above.
  * Async on `stream`. */
-int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, int8_t* k_codes,
-                            int8_t* v_codes, float* k_scales, float* v_scales, int B, int H_kv,
+int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
+                            uint8_t* v_codes, float* k_scales, float* v_scales, int B, int H_kv,
                             int S, int d, cudaStream_t stream);
 
 /* Split-KV decode over an INT8 cache: arguments, outputs, split plan,
  * workspace and errors as gqa_attn_decode, with K and V given as codes and
  * scales (S_max = the caches' S). The result is attention over the
- * dequantised cache code * scale: the kernel converts codes to f16 exactly,
+ * dequantised cache code * scale: the kernel turns each stored byte into the
+ * exact f16 value code + 1152, takes the 1152 offset off once per head, and
  * applies the K scale to each token's scores and the V scale to each token's
  * softmax weight. Rows, ragged lengths and seqlens behave as in
  * gqa_attn_decode; scales and codes beyond a row's length are never used (they
  * may hold anything). */
-int gqa_attn_decode_q8(const uint16_t* q, const int8_t* k_codes, const int8_t* v_codes,
+int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes, const uint8_t* v_codes,
                        const float* k_scales, const float* v_scales, uint16_t* o, float* lse,
                        const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max,
                        float scale, int num_splits, cudaStream_t stream);

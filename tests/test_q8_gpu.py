@@ -44,14 +44,19 @@ def _assert_close(o, lse, O_ref, L_ref, what):
         assert np.abs(l[fin] - L_ref[fin]).max() <= LSE_ABS, what
 
 
+def _stored(codes):
+    """The library's storage of int8 codes: the bytes code + 128."""
+    return (np.asarray(codes).astype(np.int16) + 128).astype(np.uint8)
+
+
 def _oracle_cache(k, v):
     """The oracle's codes and scales, in the kernel's layouts, on the GPU."""
     kc, ks = orc.quantize_q8(k)
     vc, vs = orc.quantize_q8(v)
     dev = "cuda"
     return (kc, ks, vc, vs,
-            torch.from_numpy(kc).to(dev), torch.from_numpy(np.ascontiguousarray(
-                np.swapaxes(vc, 2, 3))).to(dev),
+            torch.from_numpy(_stored(kc)).to(dev),
+            torch.from_numpy(np.ascontiguousarray(np.swapaxes(_stored(vc), 2, 3))).to(dev),
             torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev))
 
 
@@ -70,8 +75,8 @@ def test_quantiser_matches_the_oracle_bit_for_bit():
     api.check()
     okc, oks = orc.quantize_q8(k)
     ovc, ovs = orc.quantize_q8(v)
-    assert np.array_equal(kc.cpu().numpy(), okc)
-    assert np.array_equal(vc.cpu().numpy(), np.swapaxes(ovc, 2, 3))
+    assert np.array_equal(kc.cpu().numpy(), _stored(okc))
+    assert np.array_equal(vc.cpu().numpy(), np.swapaxes(_stored(ovc), 2, 3))
     assert np.array_equal(ks.cpu().numpy(), oks)
     assert np.array_equal(vs.cpu().numpy(), ovs)
     assert oks[0, 0, 5] == 1.0 and okc[0, 0, 5, 1] == 0  # rint(0.5) = 0
@@ -85,8 +90,8 @@ def test_decode_matches_the_oracle_on_ragged_rows(S_max, G):
     kc, ks, vc, vs, dkc, dvc, dks, dvs = _oracle_cache(k, v)
     # padding beyond each row's length: garbage codes and NaN scales must not leak
     for b, n in enumerate(lens):
-        dkc[b, :, n:] = 77
-        dvc[b, :, :, n:] = -91
+        dkc[b, :, n:] = 205
+        dvc[b, :, :, n:] = 37
         dks[b, :, n:] = float("nan")
         dvs[b, :, n:] = float("nan")
     sl = torch.tensor(lens, dtype=torch.int32)
@@ -105,7 +110,8 @@ def test_full_size_8k_decode_through_the_gpu_quantiser():
     api.check()
     okc, oks = orc.quantize_q8(k)
     ovc, ovs = orc.quantize_q8(v)
-    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(ks.cpu().numpy(), oks)
+    assert np.array_equal(kc.cpu().numpy(), _stored(okc))
+    assert np.array_equal(ks.cpu().numpy(), oks)
     O, L = orc.attention_q8(q, okc, oks, ovc, ovs, scale=w.scale, seqlens=sl.tolist())
     _assert_close(o, lse, O, L, "8K")
     # the quantised cache stays close to the bf16 one (information only: the
@@ -135,7 +141,7 @@ def test_ragged_128k_sampled_heads():
 
 def test_decode_rejects_unsupported_shapes():
     q = torch.zeros(1, 8, 64, dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros(1, 1, 64, 64, dtype=torch.int8, device="cuda")
+    kc = torch.zeros(1, 1, 64, 64, dtype=torch.uint8, device="cuda")
     sc = torch.zeros(1, 1, 64, device="cuda")
     with pytest.raises(api.GqaError) as e:
         api.decode_q8(q, kc, kc.clone(), sc, sc.clone())
