@@ -465,20 +465,22 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 
         } else {
             // int8 codes: K rows are tokens [TILE_T][128 B] (128-byte swizzle),
-            // V rows are head dims [D][TILE_T B] (64-byte swizzle). Each 16-key
-            // m-tile of the MMAs takes its keys in the order pi(m) = 4(m&7 >> 1)
-            // + (m & 1) + 2(m >> 3), so that a lane's B-operand keys of the P.V
-            // step (logical 2c, 2c+1, 2c+8, 2c+9) are the four consecutive
-            // codes 4c .. 4c+3 of a V row: one 32-bit load. The sum over keys
-            // does not depend on their order. Scores and P are scaled per token
-            // after the MMAs (K) and before them (V).
+            // V rows are head dims [D][TILE_T B] (64-byte swizzle). m-tile mt of
+            // the MMAs takes logical key m = 2c' + h (+8) to tile key
+            // 16c' + 4mt + h (+2), so that a lane's B-operand keys of the P.V
+            // step in every m-tile (logical 2c, 2c+1, 2c+8, 2c+9) are codes
+            // 16c + 4mt .. +3 of a V row: one 16-byte load serves all four
+            // m-tiles. The sum over keys does not depend on their order. Scores
+            // and P are scaled per token after the MMAs (K) and before them (V).
+            static_assert(TILE_T == 64, "the key order below covers 64-token tiles");
             const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
             const uint32_t vbase = kbase + C::kKBytes;
             const float* ksc = scales + (warp * STAGES + slot) * 2 * TILE_T;
             const float* vsc = ksc + TILE_T;
             const int tok0 = base + (warp + i * WARPS) * TILE_T;
             const int lo = max(tok0, r.start), hi = min(tok0 + TILE_T, r.end);
-            const int kr0 = 4 * (g >> 1) + (g & 1);  // pi(g); pi(g + 8) = kr0 + 2
+            const int kr0 = 16 * (g >> 1) + (g & 1);  // tile key of logical row g in m-tile 0;
+                                                      // row g + 8: + 2; m-tile mt: + 4 mt
 
             // ---- S^T = K_j q^T: lane c reads dims [32c, 32c + 32) of its two
             // key rows (two 16-byte chunks each) and converts them to f16.
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 uint32_t w[2][8];
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
-                    const int row = mt * 16 + kr0 + 2 * rr;
+                    const int row = 4 * mt + kr0 + 2 * rr;
 #pragma unroll
                     for (int hc = 0; hc < 2; ++hc) {
                         const uint4 v4 = ld_shared_v4(kbase + row * 128 +
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             for (int mt = 0; mt < C::kMT; ++mt) {
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
-                    const int key = mt * 16 + kr0 + 2 * rr;
+                    const int key = 4 * mt + kr0 + 2 * rr;
                     const int pos = tok0 + key;
                     ok[mt][rr] = pos >= lo && pos < hi;
                     const float f = ksc[key] * p.scale_log2;
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 // whatever scale its (padding) slot holds
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
-                    const float f = vsc[mt * 16 + kr0 + 2 * rr];
+                    const float f = vsc[4 * mt + kr0 + 2 * rr];
                     sc[mt][2 * rr] = ok[mt][rr] ? sc[mt][2 * rr] * f : 0.f;
                     sc[mt][2 * rr + 1] = ok[mt][rr] ? sc[mt][2 * rr + 1] * f : 0.f;
                 }
@@ -580,26 +582,28 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             poff0 = poff0 * corr0 + pv0;
             poff1 = poff1 * corr1 + pv1;
 
-            // ---- O^T += V_j^T P^T: lane (g, c) reads codes 4c .. 4c+3 of the
-            // 16-key group kt for dims md*16 + g and + 8.
+            // ---- O^T += V_j^T P^T: lane (g, c) reads codes 16c .. 16c+15 of dims
+            // md*16 + g and + 8 (16-byte chunk c of the 64-byte row, swizzled);
+            // word mt of each is m-tile mt's operand.
+            uint32_t b_lo[C::kMT], b_hi[C::kMT];
 #pragma unroll
             for (int kt = 0; kt < C::kMT; ++kt) {
-                const uint32_t b_lo = movmatrix_trans(pp[kt][0]);
-                const uint32_t b_hi = movmatrix_trans(pp[kt][1]);
+                b_lo[kt] = movmatrix_trans(pp[kt][0]);
+                b_hi[kt] = movmatrix_trans(pp[kt][1]);
+            }
 #pragma unroll
-                for (int md = 0; md < C::kKC; ++md) {
-                    const int d0 = md * 16 + g, d1 = d0 + 8;
-                    // the TMA swizzle of TILE_T-byte rows: the 16-byte chunk index
-                    // XOR bits 7.. of the row's byte offset
-                    constexpr int kChunkMask = TILE_T / 16 - 1;
-                    const uint32_t w0 = ld_shared_u32(
-                        vbase + d0 * TILE_T + ((kt ^ ((d0 * TILE_T >> 7) & kChunkMask)) << 4) + 4 * c);
-                    const uint32_t w1 = ld_shared_u32(
-                        vbase + d1 * TILE_T + ((kt ^ ((d1 * TILE_T >> 7) & kChunkMask)) << 4) + 4 * c);
+            for (int md = 0; md < C::kKC; ++md) {
+                const int d0 = md * 16 + g, d1 = d0 + 8;
+                const uint4 v0 = ld_shared_v4(vbase + d0 * TILE_T + ((c ^ ((d0 >> 1) & 3)) << 4));
+                const uint4 v1 = ld_shared_v4(vbase + d1 * TILE_T + ((c ^ ((d1 >> 1) & 3)) << 4));
+                const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+                const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                for (int kt = 0; kt < C::kMT; ++kt) {
                     uint32_t a[4];
-                    u8x4_to_f16x4_biased(w0, a[0], a[2]);
-                    u8x4_to_f16x4_biased(w1, a[1], a[3]);
-                    mma_f16_16816(acc[md], a, b_lo, b_hi);
+                    u8x4_to_f16x4_biased(w0[kt], a[0], a[2]);
+                    u8x4_to_f16x4_biased(w1[kt], a[1], a[3]);
+                    mma_f16_16816(acc[md], a, b_lo[kt], b_hi[kt]);
                 }
             }
         }
