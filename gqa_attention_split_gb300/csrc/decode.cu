@@ -1013,8 +1013,6 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
     return GQA_OK;
 }
 
-// Test hook (gqa_attn_debug_inject_timeout): launches left to inject.
-std::atomic<int> g_inject_timeout{0};
 
 int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse,
         const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max, float scale,
@@ -1080,11 +1078,7 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.warm_l2 = int64_t(ns) * H_kv * B <= num_sms() ? 1 : 0;  // a single wave
     sp.ring = ring ? 1 : 0;
     sp.scale_log2 = scale * kLog2e;
-    for (int n = g_inject_timeout.load(); n > 0; n = g_inject_timeout.load())
-        if (g_inject_timeout.compare_exchange_weak(n, n - 1)) {
-            sp.inject_timeout = 1;
-            break;
-        }
+    sp.inject_timeout = take_injected_timeout() ? 1 : 0;
 #ifdef GQA_TRACE
     static int trace_row = 0;  // consecutive launches get consecutive timeline rows
     if (trace_row + ns * H_kv * B > kTraceCombineBase) trace_row = 0;
@@ -1103,7 +1097,7 @@ using namespace gqa;
 
 extern "C" int gqa_attn_debug_inject_timeout(int launches) {
     if (launches < 0) return GQA_ERR_INVALID_ARG;
-    decode::g_inject_timeout.store(launches);
+    set_injected_timeouts(launches);
     return GQA_OK;
 }
 

@@ -65,6 +65,7 @@ struct Params {
     unsigned* status;
     int B, H_q, H_kv, G, T_q, S_kv, q_offset, causal, n_mblocks;
     float scale_log2;
+    int inject_timeout;  // test hook: block 0 withholds its (first) Q copy
 };
 
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -127,10 +128,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmap_q);
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
+            // Test hook: block 0 withholds its Q copy, so every wait on it runs
+            // out and reports kStatusTimeout (nothing faults, nothing hangs).
+            const bool withhold = p.inject_timeout && blockIdx.x == 0;
             const uint32_t qdst = smem_u32(smem + kQOff);
-            mbar_arrive_expect_tx(bar(kQFull), kTileBytes);
-            for (int hh = 0; hh < 2; ++hh)
-                tma_load(qdst + hh * kBoxBytes, &tmap_q, hh * 64, m0, b * p.H_q + h, bar(kQFull));
+            if (!withhold) {
+                mbar_arrive_expect_tx(bar(kQFull), kTileBytes);
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load(qdst + hh * kBoxBytes, &tmap_q, hh * 64, m0, b * p.H_q + h,
+                             bar(kQFull));
+            }
             bool alive = true;
             int issued = 0;
             for (int j = 0; j < n_tiles && alive; ++j) {
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = j + 1;
             }
             // Never leave with copies in flight into this CTA's shared memory.
-            mbar_wait_bounded(bar(kQFull), 0, p.status);
+            if (!withhold) mbar_wait_bounded(bar(kQFull), 0, p.status);
             for (int j = max(0, issued - kStages); j < issued; ++j)
                 mbar_wait_bounded(bar(kKVFull + j % kStages), (j / kStages) & 1, p.status);
         }
@@ -508,12 +515,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // Q of both heads; the previous item's last S MMAs must be done.
             if (it > 0) alive = mbar_wait_bounded(bar(pQEmpty), (it - 1) & 1, p.status);
             if (!alive) break;
-            mbar_arrive_expect_tx(bar(pQFull), 2 * kTileBytes);
-            for (int g = 0; g < 2; ++g)
-                for (int hh = 0; hh < 2; ++hh)
-                    tma_load(smem_u32(smem + kPairQOff + g * kTileBytes) + hh * kBoxBytes, &tmap_q,
-                             hh * 64, w.m0, w.b * p.H_q + w.h0 + g, bar(pQFull));
-            q_loads = it + 1;
+            // Test hook: block 0 withholds its first Q copy, so every wait on
+            // it runs out and reports kStatusTimeout (nothing faults or hangs).
+            if (!(p.inject_timeout && blockIdx.x == 0 && it == 0)) {
+                mbar_arrive_expect_tx(bar(pQFull), 2 * kTileBytes);
+                for (int g = 0; g < 2; ++g)
+                    for (int hh = 0; hh < 2; ++hh)
+                        tma_load(smem_u32(smem + kPairQOff + g * kTileBytes) + hh * kBoxBytes,
+                                 &tmap_q, hh * 64, w.m0, w.b * p.H_q + w.h0 + g, bar(pQFull));
+                q_loads = it + 1;
+            }
             for (int i = 0; i < 2 * w.n_tiles; ++i, ++r) {  // K_0, V_0, K_1, V_1, ...
                 const int s = r % kRingSlots;
                 if (r >= kRingSlots)
@@ -828,6 +839,7 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     prm.causal = causal ? 1 : 0;
     prm.n_mblocks = (T_q + BM - 1) / BM;
     prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.inject_timeout = take_injected_timeout() ? 1 : 0;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <map>
+#include <atomic>
 #include <mutex>
 #include <utility>
 
@@ -134,6 +135,17 @@ cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inn
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Test hook (gqa_attn_debug_inject_timeout): launches left to inject.
+static std::atomic<int> g_inject_timeout{0};
+
+void set_injected_timeouts(int launches) { g_inject_timeout.store(launches); }
+
+bool take_injected_timeout() {
+    for (int n = g_inject_timeout.load(); n > 0; n = g_inject_timeout.load())
+        if (g_inject_timeout.compare_exchange_weak(n, n - 1)) return true;
+    return false;
 }
 
 }  // namespace gqa

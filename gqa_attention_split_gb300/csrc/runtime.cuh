@@ -15,6 +15,10 @@ unsigned* status_word();
 
 // Current device's SM count (cached), or a negative value on failure.
 int num_sms();
+// Test hook for failure reporting: the next n launches (decode or prefill)
+// each make their first block withhold one copy (set / take one).
+void set_injected_timeouts(int launches);
+bool take_injected_timeout();
 
 // Library-owned workspace of at least `bytes` for (current device, stream).
 // Grows with stream-ordered allocation; returns nullptr on failure or when

@@ -266,10 +266,11 @@ int gqa_attn_prefill_block_n(void);
  * GQA_ERR_DEVICE_BAD_INPUT or GQA_ERR_CUDA. */
 int gqa_attn_check(cudaStream_t stream);
 
-/* Test hook for failure reporting: the next `launches` gqa_attn_decode /
- * gqa_attn_decode_ws calls each make their first block withhold its first
- * K/V copy. That block's bounded wait then runs out (after about one second),
- * the kernel records the timeout in the device status word and finishes
+/* Test hook for failure reporting: the next `launches` decode or prefill
+ * calls (gqa_attn_decode*, gqa_attn_prefill*) each make their first block
+ * withhold one copy (decode: its first K/V copy; prefill: its first Q copy).
+ * The bounded waits on it then run out (after about one second each), the
+ * kernel records the timeout in the device status word and finishes
  * normally, and gqa_attn_check() returns GQA_ERR_DEVICE_TIMEOUT. The output of
  * such a call is undefined; nothing faults and later calls are unaffected.
  * 0 disarms. Returns GQA_OK or GQA_ERR_INVALID_ARG (launches < 0). */
