@@ -679,8 +679,48 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 const float corr = need ? fast_exp2(m_run - m_new) : 1.f;
                 const float m_use = need ? m_new : m_run;
                 m_run = m_use;
+                // p = 2^(s*scale - m): sums of p and of bf16(p); P (bf16 pairs,
+                // lower key in the low half) over the first 64 columns of S.
+                const uint64_t n2 = f2pack(-m_use, -m_use);
+                uint64_t s2[4];
+                float bl[4], bh[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    s2[u] = 0ull;
+                    bl[u] = bh[u] = 0.f;
+                }
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = half * 64 + 2 * i;
+                        float x0, x1;
+                        f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), c2, n2), x0, x1);
+                        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                        s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
+                        pk[i] = pack_bf16x2(e0, e1);
+                        bl[i & 3] = add_f32_bf16_lo(bl[i & 3], pk[i]);
+                        bh[i & 3] = add_f32_bf16_hi(bh[i & 3], pk[i]);
+                    }
+                    tc::tmem_st32(lane_base + col_s + half * 32, pk);
+                }
+                {
+                    float t[8], tb[8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
+                        tb[2 * u] = bl[u];
+                        tb[2 * u + 1] = bh[u];
+                    }
+                    l_run = l_run * corr +
+                            (((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7])));
+                    lb_run = lb_run * corr + (((tb[0] + tb[1]) + (tb[2] + tb[3])) +
+                                              ((tb[4] + tb[5]) + (tb[6] + tb[7])));
+                }
                 // O is complete here: this tile's S MMA was issued after the
-                // previous P.V, and tcgen05 MMAs complete in order.
+                // previous P.V, and tcgen05 MMAs complete in order. Done after
+                // the exponentials, when the scores no longer hold registers.
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
                     const uint64_t corr2 = f2pack(corr, corr);
 #pragma unroll
@@ -700,40 +740,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         }
                         tc::tmem_st32(lane_base + col_o + c * 32, r);
                     }
-                }
-                // p = 2^(s*scale - m): sums of p and of bf16(p); P (bf16 pairs,
-                // lower key in the low half) over the first 64 columns of S.
-                const uint64_t n2 = f2pack(-m_use, -m_use);
-                uint64_t s2[4], b2[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) s2[u] = b2[u] = 0ull;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int c = half * 64 + 2 * i;
-                        float x0, x1;
-                        f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), c2, n2), x0, x1);
-                        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-                        s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
-                        pk[i] = pack_bf16x2(e0, e1);
-                        b2[i & 3] = fadd2(b2[i & 3], f2pack(__uint_as_float(pk[i] << 16),
-                                                            __uint_as_float(pk[i] & 0xFFFF0000u)));
-                    }
-                    tc::tmem_st32(lane_base + col_s + half * 32, pk);
-                }
-                {
-                    float t[8], tb[8];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
-                        f2unpack(b2[u], tb[2 * u], tb[2 * u + 1]);
-                    }
-                    l_run = l_run * corr +
-                            (((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7])));
-                    lb_run = lb_run * corr + (((tb[0] + tb[1]) + (tb[2] + tb[3])) +
-                                              ((tb[4] + tb[5]) + (tb[6] + tb[7])));
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();

@@ -322,6 +322,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// acc + the bf16 value in the low (lo) or high (hi) half of a packed pair,
+// rounded to fp32: the same sum as adding the half widened to fp32, in one
+// mixed-precision add (sm_100 and later).
+__device__ __forceinline__ float add_f32_bf16_lo(float acc, uint32_t pair) {
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+        : "=f"(d) : "r"(pair), "f"(acc));
+    return d;
+}
+__device__ __forceinline__ float add_f32_bf16_hi(float acc, uint32_t pair) {
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+        : "=f"(d) : "r"(pair), "f"(acc));
+    return d;
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a box written by
 // TMA with 128-byte swizzling (128-byte rows, 1024-byte aligned box).
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
