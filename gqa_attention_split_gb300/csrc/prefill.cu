@@ -408,7 +408,13 @@ constexpr int kPairThreads = 384;
 constexpr int kRingSlots = 4;
 constexpr uint32_t kPairQOff = 0;                                // Q_A, then Q_B
 constexpr uint32_t kPairRingOff = 2 * kTileBytes;                // kRingSlots x 32 KB
-constexpr uint32_t kPairBarOff = kPairRingOff + kRingSlots * kTileBytes;
+// O leaves through TMA stores: each softmax warp owns two 2 KB buffers, each
+// one [32 rows][32 bf16] box in the 64-byte swizzle (16-byte chunk k of row
+// r at r * 64 + ((k ^ ((r >> 1) & 3)) << 4), so a warp's row-per-lane writes
+// hit distinct banks).
+constexpr uint32_t kPairStageOff = kPairRingOff + kRingSlots * kTileBytes;
+constexpr uint32_t kStageBoxBytes = 32 * 32 * 2;
+constexpr uint32_t kPairBarOff = kPairStageOff + 8 * 2 * kStageBoxBytes;
 constexpr int kPairSmemBytes = 1024 + kPairBarOff + 256;
 static_assert(kPairSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
 static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
@@ -466,7 +472,8 @@ __device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) 
 __global__ void __launch_bounds__(kPairThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+                        const __grid_constant__ CUtensorMap tmap_v,
+                        const __grid_constant__ CUtensorMap tmap_o, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -633,6 +640,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
         const uint32_t col_s = col_s_of(g), col_o = col_o_of(g);
+        const uint32_t stage = smem_u32(smem + kPairStageOff + (g * 4 + quad) * 2 * kStageBoxBytes);
         const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
         bool alive = true;
         int tt = 0;  // KV tiles finished so far, over all work items
@@ -762,26 +770,37 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 uint32_t r[32];
                 tc::tmem_ld32(lane_base + col_o + c * 32, r);
                 tc::tmem_wait_ld();
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + c * 32);
+                // buffer c & 1 was last read by the store two chunks back
+                const uint32_t buf = stage + (c & 1) * kStageBoxBytes;
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv,
-                                           __uint_as_float(r[v4 * 8 + 1]) * inv);
-                        o4.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv,
-                                           __uint_as_float(r[v4 * 8 + 3]) * inv);
-                        o4.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv,
-                                           __uint_as_float(r[v4 * 8 + 5]) * inv);
-                        o4.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv,
-                                           __uint_as_float(r[v4 * 8 + 7]) * inv);
-                        dst[v4] = o4;
-                    }
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    uint4 o4;
+                    o4.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv,
+                                       __uint_as_float(r[v4 * 8 + 1]) * inv);
+                    o4.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv,
+                                       __uint_as_float(r[v4 * 8 + 3]) * inv);
+                    o4.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv,
+                                       __uint_as_float(r[v4 * 8 + 5]) * inv);
+                    o4.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv,
+                                       __uint_as_float(r[v4 * 8 + 7]) * inv);
+                    st_shared_v4(buf + lane * 64 + ((v4 ^ ((lane >> 1) & 3)) << 4), o4);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    // rows at or past T_q fall outside the tensor and are not written
+                    tma_store_3d(&tmap_o, buf, c * 32, w.m0 + quad * 32,
+                                 w.b * p.H_q + w.h0 + g);
+                    bulk_commit_group();
                 }
             }
             if (valid && p.lse) p.lse[orow] = (m_run + __log2f(l_run)) * kLn2;
             tt += w.n_tiles;
         }
+        // the O stores finish before the CTA (and its shared memory) does
+        if (lane == 0) bulk_wait_group_all();
     }
 
     tc::fence_before_sync();
@@ -823,7 +842,7 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     if (B == 0 || T_q == 0) return GQA_OK;
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (encode_tmap_3d_bf16(&tq, q, D, T_q, uint64_t(B) * H_q, 64, BM,
                             CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
         encode_tmap_3d_bf16(&tk, k, D, S_kv, uint64_t(B) * H_kv, 64, BN,
@@ -863,8 +882,11 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     if (pair) {
         // persistent: one CTA per SM (at most one per work item)
         const int ctas = int(items < int64_t(num_sms()) ? items : int64_t(num_sms()));
+        if (encode_tmap_3d_bf16(&to, o, D, T_q, uint64_t(B) * H_q, 32, 32,
+                                CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess)
+            return GQA_ERR_CUDA;
         prefill_pair_kernel<<<dim3(unsigned(ctas)), kPairThreads, kPairSmemBytes, stream>>>(
-            tq, tk, tv, prm);
+            tq, tk, tv, to, prm);
     }
     else
         prefill_kernel<<<dim3(unsigned(items)), kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
