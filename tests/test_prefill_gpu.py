@@ -65,6 +65,21 @@ def test_small_shapes(B, H_q, H_kv, T_q, S_kv, off, causal):
     assert_close(o, lse, O, L, f"B={B} H={H_q}/{H_kv} T={T_q} S={S_kv} off={off} c={causal}")
 
 
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_a_later_tile_with_much_larger_scores(causal):
+    # Keys 256..383 scaled by 8 (exact in bf16): from the third KV tile on, the
+    # running max of each row that sees them grows by far more than the rescale
+    # threshold, so O and the sums are rescaled mid-row; the fourth tile then
+    # runs against that larger max.
+    B, H_q, H_kv, T, S = 1, 8, 2, 512, 512
+    q, k, v = wl.small_prefill(B, H_q, H_kv, 128, T, S, 0, seed=77)
+    k = k.clone()
+    k[:, :, 256:384] *= 8
+    o, lse = run_prefill(q, k, v, 0, causal)
+    O, L = orc.attention(q, k, v, scale=1 / math.sqrt(128), causal=causal)
+    assert_close(o, lse, O, L, f"large scores causal={causal}")
+
 def _sample_rows(B, H_q, T_q, n, seed):
     rng = np.random.default_rng(seed)
     rows = {(0, 0, 0), (B - 1, H_q - 1, T_q - 1), (0, H_q // 2, min(127, T_q - 1)),
