@@ -45,6 +45,7 @@ _SIGNATURES = {
     "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_prefill_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_pick_num_splits": (_I, [_I, _I, _I, _I]),
+    "gqa_attn_pick_num_splits_q8": (_I, [_I, _I, _I, _I]),
     "gqa_attn_decode_cluster_size": (_I, [_I, _I, _I, _I]),
     "gqa_attn_split_bounds": (_I, [_I, _I, _I, _P, _P]),
     "gqa_attn_tile_class": (_I, [_I, _I, _I, _I]),
@@ -132,6 +133,10 @@ def gqa_attn_prefill_ex(q, k, v, o, lse, B, H_q, H_kv, d, T_q, S_kv, q_offset, c
 
 def gqa_attn_pick_num_splits(B, H_kv, S_max, num_sms):
     return lib().gqa_attn_pick_num_splits(B, H_kv, S_max, num_sms)
+
+
+def gqa_attn_pick_num_splits_q8(B, H_kv, S_max, num_sms):
+    return lib().gqa_attn_pick_num_splits_q8(B, H_kv, S_max, num_sms)
 
 
 def gqa_attn_decode_cluster_size(B, H_kv, num_splits, num_sms):

@@ -1341,7 +1341,7 @@ extern "C" int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes,
     if (ns == 0) {
         const int sms = num_sms();
         if (sms <= 0) return GQA_ERR_CUDA;
-        ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
+        ns = gqa_attn_pick_num_splits_q8(B, H_kv, S_max, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
     const size_t bytes = decode::ws_layout(B, H_q, d, ns,

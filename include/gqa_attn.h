@@ -187,7 +187,8 @@ int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, uint8_t* k_cod
                             int S, int d, cudaStream_t stream);
 
 /* Split-KV decode over an INT8 cache: arguments, outputs, split plan,
- * workspace and errors as gqa_attn_decode, with K and V given as codes and
+ * workspace and errors as gqa_attn_decode (num_splits == 0 resolved with
+ * gqa_attn_pick_num_splits_q8), with K and V given as codes and
  * scales (S_max = the caches' S). The result is attention over the
  * dequantised cache code * scale: the kernel turns each stored byte into the
  * exact f16 value code + 1152, takes the 1152 offset off once per head, and
@@ -231,6 +232,12 @@ int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * most max(1, S_max / 256) so no split is shorter than 256 keys. Returns
  * >= 1, or GQA_ERR_INVALID_ARG. */
 int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
+
+/* Split count for a decode over an INT8 cache: gqa_attn_pick_num_splits for a
+ * row of ceil(S_max / 2) keys. The split-length bounds above are sized in
+ * bytes, and an INT8 token (2 x d code bytes + 2 fp32 scales) is about half
+ * a bf16 token (4 x d bytes). Returns >= 1, or GQA_ERR_INVALID_ARG. */
+int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_sms);
 
 /* Cluster size a decode launch uses on a GPU with num_sms SMs: the largest of
  * 16, 8, 4, 2 that divides num_splits (else 1), at most 8 when the grid of

@@ -113,6 +113,17 @@ def test_pick_num_splits_bit_exact_and_properties(L):
     assert api.gqa_attn_pick_num_splits(0, 8, 8192, 152) == api.GQA_ERR_INVALID_ARG
 
 
+def test_pick_num_splits_q8_plans_half_the_keys(L):
+    # an INT8 token is about half the bytes of a bf16 one
+    assert api.gqa_attn_pick_num_splits_q8(1, 8, 8192, 152) == 16     # 8K decode: unchanged
+    assert api.gqa_attn_pick_num_splits_q8(4, 8, 131072, 152) == 64   # 128K ragged: half
+    for B, H_kv, S, sms in itertools.product((1, 4, 64), (1, 8), (1, 2, 255, 513, 8192, 131072),
+                                             (1, 152)):
+        assert api.gqa_attn_pick_num_splits_q8(B, H_kv, S, sms) == \
+            _pick_reference(B, H_kv, -(-S // 2), sms), (B, H_kv, S, sms)
+    assert api.gqa_attn_pick_num_splits_q8(1, 8, 0, 152) == api.GQA_ERR_INVALID_ARG
+
+
 def test_decode_cluster_size(L):
     # largest of 16, 8, 4, 2 dividing the split count; at most 8 once the grid
     # (splits x KV heads x batch) has more CTAs than SMs
