@@ -445,6 +445,32 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// MMAs with the descriptors given as 32-bit halves: the k-steps of one
+// operand differ only in the start-address field of the low word, so each
+// step adds to the low word alone; kAcc fixed at compile time needs no flag.
+template <int kAcc>
+__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(kAcc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // One work item: a 128-row query block of two adjacent query heads of one
 // KV group. Items are numbered heaviest first (query blocks from the last
 // one down), and a CTA takes items c, 2G-1-c, 2G+c, ... (snake order).
@@ -571,20 +597,25 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         auto issue_s = [&](int g, int ri) {  // S_g = Q_g K^T, K in ring item ri
             const uint64_t qdesc = g ? qdesc1 : qdesc0;
             const uint64_t kdesc = tc::sdesc_sw128(slot_addr(ri), 16, 1024);
+            const uint32_t qlo = uint32_t(qdesc), qhi = uint32_t(qdesc >> 32);
+            const uint32_t klo = uint32_t(kdesc), khi = uint32_t(kdesc >> 32);
+            const uint32_t dst = tmem + col_s_of(g);
+            mma_ss_lo<0>(dst, qlo, qhi, klo, khi, idesc_s);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-                tc::mma_ss(tmem + col_s_of(g), qdesc + off, kdesc + off, idesc_s, kk > 0);
+            for (int kk = 1; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                mma_ss_lo<1>(dst, qlo + off, qhi, klo + off, khi, idesc_s);
             }
             tc::commit(bar(pSFull + g));
         };
         auto issue_pv = [&](int g, int ri, bool first) {  // O_g (+)= P_g V, V in ring item ri
             const uint64_t vdesc = tc::sdesc_sw128(slot_addr(ri), kBoxBytes, 1024);
+            const uint32_t vlo = uint32_t(vdesc), vhi = uint32_t(vdesc >> 32);
+            const uint32_t dst = tmem + col_o_of(g), src = tmem + col_s_of(g);
+            mma_ts_lo(dst, src, vlo, vhi, idesc_pv, first ? 0u : 1u);
 #pragma unroll
-            for (int ks = 0; ks < BN / 16; ++ks)
-                mma_ts(tmem + col_o_of(g), tmem + col_s_of(g) + ks * 8,
-                       vdesc + uint64_t((ks * 2048) >> 4), idesc_pv,
-                       (!first || ks > 0) ? 1u : 0u);
+            for (int ks = 1; ks < BN / 16; ++ks)
+                mma_ts_lo(dst, src + ks * 8, vlo + uint32_t((ks * 2048) >> 4), vhi, idesc_pv, 1u);
         };
         bool alive = true;
         int r = 0;   // ring items consumed so far
