@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             return smem_u32(smem + kPairRingOff + (i % kRingSlots) * kTileBytes);
         };
         auto wait_item = [&](int i) {
-            return mbar_wait_fast(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1, p.status);
+            return mbar_wait_bounded(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1, p.status);
         };
         // Descriptors are built once per operand; each k-step adds its byte
         // offset >> 4 to the 14-bit start-address field (shared addresses
@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         int tt = 0;  // KV tiles finished so far (S and P barrier phases)
         for (int it = 0; alive && pair_item(p, it, w); ++it) {
             const int n = w.n_tiles;
-            alive = mbar_wait_fast(bar(pQFull), it & 1, p.status) && wait_item(r);
+            alive = mbar_wait_bounded(bar(pQFull), it & 1, p.status) && wait_item(r);
             if (!alive) break;
             tc::fence_after_sync();
             issue_s(0, r);
@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     // P_g(0) of an item is written after the softmax threads
                     // have read the previous item's O_g, so PV_g(0) may
                     // overwrite it.
-                    alive = mbar_wait_fast(bar(pPFull + g), (tt + j) & 1, p.status);
+                    alive = mbar_wait_bounded(bar(pPFull + g), (tt + j) & 1, p.status);
                     if (!alive) break;
                     tc::fence_after_sync();
                     issue_pv(g, rv, j == 0);
@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
             for (int j = 0; j < w.n_tiles && alive; ++j) {
                 alive = __all_sync(0xffffffffu,
-                                   mbar_wait_fast(bar(pSFull + g), (tt + j) & 1, p.status));
+                                   mbar_wait_bounded(bar(pSFull + g), (tt + j) & 1, p.status));
                 if (!alive) break;
                 tc::fence_after_sync();
                 float sv[BN];
@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // ---- epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2. Every
             // read of O_g completes (wait::ld) before this warp's next P
             // arrive, which is what lets the next item's PV_g(0) overwrite O_g.
-            alive = __all_sync(0xffffffffu, mbar_wait_fast(bar(pODone + g), it & 1, p.status));
+            alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pODone + g), it & 1, p.status));
             if (!alive) break;
             tc::fence_after_sync();
             const bool valid = w.m0 + row < p.T_q;

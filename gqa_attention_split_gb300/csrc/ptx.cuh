@@ -62,61 +62,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe of phase `parity`.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// try_wait with an explicit bound on how long the thread may stay suspended.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-#ifndef GQA_FAST_WAIT_MODE
-#define GQA_FAST_WAIT_MODE 1
-#endif
-// Wait on a barrier that sits on a latency-critical path: a plain try_wait
-// can stay suspended for a long time slice after the phase completes, so
-// this polls (test_wait, mode 2) or bounds each suspension (mode 1) instead.
-// Same bounded semantics as mbar_wait_bounded.
-__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, unsigned* status) {
-    unsigned long long t0 = 0;
-    for (uint32_t i = 1;; ++i) {
-#if GQA_FAST_WAIT_MODE == 2
-        if (mbar_test_wait(bar, parity)) return true;
-#elif GQA_FAST_WAIT_MODE == 1
-        if (mbar_try_wait_hint(bar, parity, 40)) return true;
-#else
-        if (mbar_try_wait(bar, parity)) return true;
-#endif
-        if ((i & 1023u) == 0) {
-            const unsigned long long t = globaltimer();
-            if (t0 == 0) {
-                t0 = t;
-            } else if (t - t0 > kWaitLimitNs) {
-                atomicOr(status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
 // Waits for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
 // On expiry it sets kStatusTimeout in *status and returns false; the caller
 // then stops waiting (and stops issuing work) but still runs to the end.
