@@ -77,6 +77,33 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// MMAs with the descriptors given as 32-bit halves: the k-steps of one
+// operand differ only in the start-address field of the low word, so each
+// step adds to the low word alone; kAcc fixed at compile time needs no flag.
+template <int kAcc>
+__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(kAcc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
@@ -167,6 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false);
             const uint32_t idesc_pv = tc::idesc_bf16_f32(BM, D, true);
             const uint32_t qsm = smem_u32(smem + kQOff), psm = smem_u32(smem + kPOff);
+            // Descriptors are built once per operand; each k-step adds its byte
+            // offset >> 4 to the start-address field of the low word (shared
+            // addresses stay below 256 KB, so the field never carries out).
+            const uint64_t qdesc = tc::sdesc_sw128(qsm, 16, 1024);
+            const uint64_t pdesc = tc::sdesc_sw128(psm, 16, 1024);
+            const uint32_t qlo = uint32_t(qdesc), qhi = uint32_t(qdesc >> 32);
+            const uint32_t plo = uint32_t(pdesc), phi = uint32_t(pdesc >> 32);
             bool alive = mbar_wait_bounded(bar(kQFull), 0, p.status);
             for (int j = 0; j <= n_tiles && alive; ++j) {
                 if (j < n_tiles) {
@@ -178,11 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!alive) break;
                     tc::fence_after_sync();
                     const uint32_t ksm = smem_u32(smem + kKVOff + s * 2 * kTileBytes);
+                    const uint64_t kdesc = tc::sdesc_sw128(ksm, 16, 1024);
+                    const uint32_t klo = uint32_t(kdesc), khi = uint32_t(kdesc >> 32);
+                    const uint32_t dst = tmem + (j & 1) * BN;
+                    mma_ss_lo<0>(dst, qlo, qhi, klo, khi, idesc_s);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                        tc::mma_ss(tmem + (j & 1) * BN, tc::sdesc_sw128(qsm + off, 16, 1024),
-                                   tc::sdesc_sw128(ksm + off, 16, 1024), idesc_s, kk > 0);
+                    for (int kk = 1; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                        mma_ss_lo<1>(dst, qlo + off, qhi, klo + off, khi, idesc_s);
                     }
                     tc::commit(bar(kSFull + (j & 1)));
                 }
@@ -192,12 +229,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!alive) break;
                     tc::fence_after_sync();
                     const uint32_t vsm = smem_u32(smem + kKVOff + s * 2 * kTileBytes + kTileBytes);
+                    const uint64_t vdesc = tc::sdesc_sw128(vsm, kBoxBytes, 1024);
+                    const uint32_t vlo = uint32_t(vdesc), vhi = uint32_t(vdesc >> 32);
+                    if (jp > 0)
+                        mma_ss_lo<1>(tmem + kTmemO, plo, phi, vlo, vhi, idesc_pv);
+                    else
+                        mma_ss_lo<0>(tmem + kTmemO, plo, phi, vlo, vhi, idesc_pv);
 #pragma unroll
-                    for (int ks = 0; ks < BN / 16; ++ks) {
-                        const uint32_t aoff = (ks >> 2) * kBoxBytes + (ks & 3) * 32;
-                        tc::mma_ss(tmem + kTmemO, tc::sdesc_sw128(psm + aoff, 16, 1024),
-                                   tc::sdesc_sw128(vsm + ks * 2048, kBoxBytes, 1024), idesc_pv,
-                                   (jp > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 1; ks < BN / 16; ++ks) {
+                        const uint32_t aoff = ((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4;
+                        mma_ss_lo<1>(tmem + kTmemO, plo + aoff, phi, vlo + ((ks * 2048) >> 4), vhi,
+                                     idesc_pv);
                     }
                     tc::commit(bar(kPVDone));
                     tc::commit(bar(kKVEmpty + s));
@@ -272,9 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
                 const uint64_t n2 = f2pack(-m_use, -m_use);
-                uint64_t s2[4], b2[4];
+                uint64_t s2[4];
+                float bl[4], bh[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) s2[u] = b2[u] = 0ull;
+                for (int u = 0; u < 4; ++u) {
+                    s2[u] = 0ull;
+                    bl[u] = bh[u] = 0.f;
+                }
 #pragma unroll
                 for (int i = 0; i < BN / 2; ++i) {
                     float x0, x1;
@@ -282,14 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
                     s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
                     pk[i] = pack_bf16x2(e0, e1);
-                    b2[i & 3] = fadd2(b2[i & 3], f2pack(__uint_as_float(pk[i] << 16),
-                                                        __uint_as_float(pk[i] & 0xFFFF0000u)));
+                    bl[i & 3] = add_f32_bf16_lo(bl[i & 3], pk[i]);
+                    bh[i & 3] = add_f32_bf16_hi(bh[i & 3], pk[i]);
                 }
                 float t[8], tb[8];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
-                    f2unpack(b2[u], tb[2 * u], tb[2 * u + 1]);
+                    tb[2 * u] = bl[u];
+                    tb[2 * u + 1] = bh[u];
                 }
                 const float rs = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
                 const float rsb =
@@ -442,32 +489,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// MMAs with the descriptors given as 32-bit halves: the k-steps of one
-// operand differ only in the start-address field of the low word, so each
-// step adds to the low word alone; kAcc fixed at compile time needs no flag.
-template <int kAcc>
-__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "mov.b64 da, {%1, %2};\n\t"
-        "mov.b64 db, {%3, %4};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(kAcc)
-        : "memory");
-}
-__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "mov.b64 db, {%2, %3};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
