@@ -438,13 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // item's epilogue, and the tensor memory is allocated once.
 //   warpgroup 0 (104 registers/thread): warp 0 TMA (per item: Q of both heads,
 //               then K_j, V_j through a 4-slot ring); warp 1 owns the tensor
-//               memory; warps 1 and 2 each issue one head's MMAs, per KV tile
-//               j: PV_g(j) then S_g(j+1). An S MMA overwrites the P its
-//               thread's previous PV read; the tcgen05.mma operations of one
-//               thread execute in issue order. Warp 3 only waits.
+//               memory and one thread of it issues every MMA, per KV tile j:
+//               PV_A(j), S_A(j+1), PV_B(j), S_B(j+1). An S MMA overwrites the
+//               P the previous PV of its head read; the tcgen05.mma operations
+//               of one thread execute and complete in issue order. Warps 2
+//               and 3 only wait.
 //   warpgroups 1 and 2 (200 registers/thread): softmax of head A and of
-//               head B, then that head's epilogue; while one group computes,
-//               the tensor core runs the other group's MMAs.
+//               head B, then that head's epilogue (O through TMA stores);
+//               while one group computes, the tensor core runs the other
+//               group's MMAs.
 // Register split: 128 x 104 + 256 x 200 = 64512 = 384 threads x 168 at launch.
 // Every barrier phase is counted across items: the k-th completion of a
 // barrier has parity k & 1.
@@ -471,9 +473,9 @@ __device__ __forceinline__ uint32_t col_o_of(int g) { return 256u + uint32_t(g) 
 
 enum PairBar {
     pQFull = 0,                        // Q of both heads landed (per item)
-    pQEmpty = 1,                       // both issuers are done with Q (count 2)
+    pQEmpty = 1,                       // the item's last S MMAs have completed
     pSlotFull = 2,                     // x kRingSlots
-    pSlotEmpty = pSlotFull + kRingSlots,  // x kRingSlots, released by both issuers
+    pSlotEmpty = pSlotFull + kRingSlots,  // x kRingSlots, released by the MMA thread's commits
     pSFull = pSlotEmpty + kRingSlots,  // x2: S_g ready (per tile)
     pPFull = pSFull + 2,               // x2: P_g ready (4 softmax warps)
     pODone = pPFull + 2,               // x2: O_g final (per item)
