@@ -968,7 +968,7 @@ template <int D, bool Q8>
 int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     int rc;
     if constexpr (Q8)
-        rc = sp.warm_l2 ? launch_cs<D, true, 2, 3>(sp, cs, maps, stream)
+        rc = sp.warm_l2 ? launch_cs<D, true, 4, 1>(sp, cs, maps, stream)
                         : launch_cs<D, true, 3, 2>(sp, cs, maps, stream);
     else
         rc = launch_cs<D, false, kWarps, kStages>(sp, cs, maps, stream);
