@@ -971,7 +971,8 @@ int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStre
         rc = sp.warm_l2 ? launch_cs<D, true, 4, 1>(sp, cs, maps, stream)
                         : launch_cs<D, true, 3, 2>(sp, cs, maps, stream);
     else
-        rc = launch_cs<D, false, kWarps, kStages>(sp, cs, maps, stream);
+        rc = sp.warm_l2 ? launch_cs<D, false, kWarps, kStages>(sp, cs, maps, stream)
+                        : launch_cs<D, false, 4, 1>(sp, cs, maps, stream);
     if (rc != GQA_OK || sp.n_groups == 1) return rc;
 
     static bool attr_set = false;
