@@ -57,6 +57,8 @@ def run_prefill(q, k, v, q_offset, causal, scale=None):
     (1, 6, 2, 257, 300, 43, True),      # odd G = 3 (one head per CTA), chunk at an offset
     (1, 16, 2, 128, 640, 0, False),     # full attention over more keys than queries
     (3, 8, 1, 129, 129, 0, True),       # three batch rows, one query row past a block
+    (1, 8, 2, 1, 1000, 999, True),      # one query at the end of a long prefix (causal)
+    (2, 8, 2, 1, 777, 0, False),        # one query, full attention over ragged keys
 ])
 def test_small_shapes(B, H_q, H_kv, T_q, S_kv, off, causal):
     q, k, v = wl.small_prefill(B, H_q, H_kv, 128, T_q, S_kv, off, seed=10 + T_q + S_kv)
