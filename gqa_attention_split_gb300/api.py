@@ -54,6 +54,7 @@ _SIGNATURES = {
     "gqa_attn_prefill_block_n": (_I, []),
     "gqa_attn_check": (_I, [_P]),
     "gqa_attn_debug_inject_timeout": (_I, [_I]),
+    "gqa_attn_debug_tile_counts": (_I, [_P, _I]),
     "gqa_attn_strerror": (ctypes.c_char_p, [_I]),
     "gqa_attn_version": (_I, []),
 }
@@ -68,6 +69,22 @@ class GqaError(RuntimeError):
         super().__init__(f"{where}: {strerror(code)} (code {code})")
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Loads a build of the library at ``path`` with every signature set.
+    ``lib()`` uses it for the product library; tests use it for the debug
+    build (``build.build(debug=True)``), which loads beside it."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with "
+            "`python -m gqa_attention_split_gb300.build` (CUDA 13, sm_103a)")
+    L = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """Loads libgqa_attn.so (once). Raises if it has not been built."""
     global _lib
@@ -75,16 +92,7 @@ def lib() -> ctypes.CDLL:
         return _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(
-                    f"{LIB_PATH} is missing: build it with "
-                    "`python -m gqa_attention_split_gb300.build` (CUDA 13, sm_103a)")
-            L = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in _SIGNATURES.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = load(LIB_PATH)
     return _lib
 
 
@@ -177,6 +185,14 @@ def gqa_attn_check(stream=None):
 
 def gqa_attn_debug_inject_timeout(launches):
     return lib().gqa_attn_debug_inject_timeout(launches)
+
+
+def gqa_attn_debug_tile_counts(clear=False, L=None):
+    """Returns (rc, [all_past, partial, all_future]) from ``L`` (default: the
+    product library, whose non-debug build returns GQA_ERR_UNSUPPORTED)."""
+    c = (ctypes.c_int64 * 3)()
+    rc = (L or lib()).gqa_attn_debug_tile_counts(c, 1 if clear else 0)
+    return rc, [c[0], c[1], c[2]]
 
 
 def strerror(code: int) -> str:

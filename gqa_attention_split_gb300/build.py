@@ -4,7 +4,7 @@ Every translation unit compiles in parallel to ``_build/`` at the repository
 root; the shared library lands next to this file. A rebuild happens only when
 a source or header is newer than the library.
 
-    python -m gqa_attention_split_gb300.build [--force] [--verbose]
+    python -m gqa_attention_split_gb300.build [--force] [--verbose] [--debug]
 """
 
 from __future__ import annotations
@@ -22,6 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgqa_attn.so")
+DEBUG_LIB = os.path.join(PKG, "libgqa_attn_debug.so")
 
 SOURCES = ["plan.cpp", "runtime.cu", "decode.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -44,15 +45,23 @@ def _newest_input() -> float:
     return max(t, os.path.getmtime(__file__))
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          debug: bool = False) -> str:
+    """Builds the library; ``debug=True`` builds the -DGQA_DEBUG variant
+    (``libgqa_attn_debug.so``, with the prefill tile counters) instead.
+    Returns the library's path."""
+    lib = DEBUG_LIB if debug else LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    out_dir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(out_dir, exist_ok=True)
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(out_dir, src + ".o")
         extra = os.environ.get("GQA_EXTRA_NVCC_FLAGS", "").split()
+        if debug:
+            extra.append("-DGQA_DEBUG")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_verbose and src.endswith(".cu"):
             cmd.insert(1, "-Xptxas=-v")
@@ -67,13 +76,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
@@ -81,5 +90,6 @@ if __name__ == "__main__":
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-verbose", action="store_true")
+    ap.add_argument("--debug", action="store_true", help="the -DGQA_DEBUG variant")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose, ptxas_verbose=a.ptxas_verbose))
+    print(build(force=a.force, verbose=a.verbose, ptxas_verbose=a.ptxas_verbose, debug=a.debug))

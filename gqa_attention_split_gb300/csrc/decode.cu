@@ -330,25 +330,51 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // q^T as the B operand (k = head dim, n = query head g of this group).
     // int8: f16 pairs, with the head dims in the order the K words are read
     // (k step kc of lane c takes dims 32c + 4kc .. +3; see the S MMA below).
+    // Before the conversion each head is scaled by a power of two 2^e that puts
+    // its largest |q| in [2^14, 2^15): the f16 operands then hold every bf16 bit
+    // of q whatever its magnitude (unscaled, |q| > 65504 would overflow f16 and
+    // tiny q would fall into its subnormals). 2^-e comes off with the K scale.
     uint32_t qf[C::kKC][2];
-    float qsum = 0.f;  // int8: this lane's share of sum_d q[g][d] (f16 values)
+    float qsum = 0.f;  // int8: this lane's share of sum_d q[g][d] (scaled f16 values)
+    [[maybe_unused]] float hs0 = p.scale_log2, hs1 = p.scale_log2;  // int8: heads 2c, 2c+1
     {
         const bool has = g < p.G;
         const uint16_t* qh = p.q + (size_t(b) * p.H_q + kv * p.G + (has ? g : 0)) * D;
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qh);
+        if constexpr (Q8) {
+            uint2 w[C::kKC];
+            float amax = 0.f;
 #pragma unroll
-        for (int kc = 0; kc < C::kKC; ++kc) {
-            if constexpr (Q8) {
-                const uint2 w = has ? *reinterpret_cast<const uint2*>(qh + 32 * c + 4 * kc)
-                                    : make_uint2(0u, 0u);
-                qf[kc][0] = pack_f16x2(__uint_as_float(w.x << 16),
-                                       __uint_as_float(w.x & 0xFFFF0000u));
-                qf[kc][1] = pack_f16x2(__uint_as_float(w.y << 16),
-                                       __uint_as_float(w.y & 0xFFFF0000u));
+            for (int kc = 0; kc < C::kKC; ++kc) {
+                w[kc] = has ? *reinterpret_cast<const uint2*>(qh + 32 * c + 4 * kc)
+                            : make_uint2(0u, 0u);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(w[kc].x << 16)),
+                                               fabsf(__uint_as_float(w[kc].x & 0xFFFF0000u))),
+                                         fmaxf(fabsf(__uint_as_float(w[kc].y << 16)),
+                                               fabsf(__uint_as_float(w[kc].y & 0xFFFF0000u)))));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));  // head g's max |q|
+            // amax in [2^(E-127), 2^(E-126)) for a normal amax with exponent field E
+            const int ebits = int((__float_as_uint(amax) >> 23) & 0xffu);
+            const int e = amax > 0.f ? min(max(141 - ebits, -126), 126) : 0;
+            const float up = __uint_as_float(uint32_t(e + 127) << 23);    // 2^e
+            const float down = __uint_as_float(uint32_t(127 - e) << 23);  // 2^-e
+#pragma unroll
+            for (int kc = 0; kc < C::kKC; ++kc) {
+                qf[kc][0] = pack_f16x2(__uint_as_float(w[kc].x << 16) * up,
+                                       __uint_as_float(w[kc].x & 0xFFFF0000u) * up);
+                qf[kc][1] = pack_f16x2(__uint_as_float(w[kc].y << 16) * up,
+                                       __uint_as_float(w[kc].y & 0xFFFF0000u) * up);
                 const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][0]));
                 const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][1]));
                 qsum += (f0.x + f0.y) + (f1.x + f1.y);
-            } else {
+            }
+            hs0 = p.scale_log2 * __shfl_sync(0xffffffffu, down, 8 * c);      // head 2c
+            hs1 = p.scale_log2 * __shfl_sync(0xffffffffu, down, 8 * c + 4);  // head 2c + 1
+        } else {
+#pragma unroll
+            for (int kc = 0; kc < C::kKC; ++kc) {
                 qf[kc][0] = has ? qrow[(kc * 16 + 2 * c) / 2] : 0u;
                 qf[kc][1] = has ? qrow[(kc * 16 + 8 + 2 * c) / 2] : 0u;
             }
@@ -521,11 +547,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                     const int key = 4 * mt + kr0 + 2 * rr;
                     const int pos = tok0 + key;
                     ok[mt][rr] = pos >= lo && pos < hi;
-                    const float f = ksc[key] * p.scale_log2;
+                    const float kq = ksc[key];  // the token's K scale
                     sc[mt][2 * rr] =
-                        ok[mt][rr] ? (sc[mt][2 * rr] - qoff0) * f : -INFINITY;
+                        ok[mt][rr] ? (sc[mt][2 * rr] - qoff0) * (kq * hs0) : -INFINITY;
                     sc[mt][2 * rr + 1] =
-                        ok[mt][rr] ? (sc[mt][2 * rr + 1] - qoff1) * f : -INFINITY;
+                        ok[mt][rr] ? (sc[mt][2 * rr + 1] - qoff1) * (kq * hs1) : -INFINITY;
                 }
                 mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
                 mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
@@ -918,8 +944,10 @@ int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream
     constexpr int kT = Q8 ? kTileTQ8 : kTileT;
     using C = SplitCfg<D, kT, kS, kW, Q8>;
     auto kern = split_kernel<D, kT, kS, kW, CS, Q8>;
-    static bool attr_set = false;  // benign race: setting it twice is harmless
-    if (!attr_set) {
+    // once per device (a race only sets them twice, which is harmless)
+    static std::atomic<uint64_t> attr_done{0};
+    const int dev = current_device();
+    if (device_attrs_pending(attr_done, dev)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
@@ -929,7 +957,7 @@ int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
                 cudaSuccess)
             return GQA_ERR_CUDA;
-        attr_set = true;
+        device_attrs_mark(attr_done, dev);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sp.ns, sp.H_kv, sp.B);
@@ -975,12 +1003,13 @@ int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStre
                         : launch_cs<D, false, 4, 1>(sp, cs, maps, stream);
     if (rc != GQA_OK || sp.n_groups == 1) return rc;
 
-    static bool attr_set = false;
-    if (!attr_set) {
+    static std::atomic<uint64_t> attr_done{0};
+    const int dev = current_device();
+    if (device_attrs_pending(attr_done, dev)) {
         if (cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  100) != cudaSuccess)
             return GQA_ERR_CUDA;
-        attr_set = true;
+        device_attrs_mark(attr_done, dev);
     }
     CombineParams cp{sp.part_o, sp.part_m, sp.part_l, sp.seqlens, sp.o, sp.lse,
                      sp.B, sp.H_q, sp.S_max, sp.n_groups, int64_t(cs) * sp.L};
@@ -1379,48 +1408,35 @@ extern "C" int gqa_attn_trace_dump(void* host, size_t bytes, int clear) {
 // once at start-up and forbids later allocations, a host that routes every
 // device byte through its own allocator, or a latency-critical path that
 // cannot afford cudaMalloc's implicit device synchronisation. For them the
-// split-KV decode above runs with its scratch (the per-cluster partials and a
-// status word) in fixed arrays that live in this library's module: every GPU
-// that loads the library holds them until the process exits.
-
-#include <mutex>
+// split-KV decode above runs with the scratch of its split merge (the
+// per-cluster partials) in a fixed array that lives in this library's module:
+// every GPU that loads the library holds it until the process exits. The
+// status word is the library's own (also module memory), so gqa_attn_check()
+// reports this entry point's device errors without allocating either.
 
 namespace gqa {
 namespace decode {
 
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static_assert(kNoAllocScratchBytes == GQA_NOALLOC_SCRATCH_BYTES, "header limit");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-static __device__ unsigned g_noalloc_status;
 
-struct NoAllocDevice {
-    bool ready;
-    void* scratch;     // device address of g_noalloc_scratch on this device
-    unsigned* status;  // device address of g_noalloc_status on this device
-};
 constexpr int kNoAllocMaxDevices = 64;
-static NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];  // zero-initialised, no heap
-static std::mutex g_noalloc_mu;
+static std::atomic<void*> g_noalloc_addr[kNoAllocMaxDevices];  // zero-initialised, no heap
 
-// Looks up the device addresses of the two arrays once per device (with that
-// device current). In host code the array names are host-side stand-ins, not
-// device addresses, so they must never be passed to a kernel directly.
-static int noalloc_setup(void** scratch, unsigned** status) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return GQA_ERR_CUDA;
+// Looks up the device address of the array once per device (with that device
+// current). In host code the array's name is a host-side stand-in, not a
+// device address, so it must never be passed to a kernel directly.
+static int noalloc_scratch(void** scratch) {
+    const int dev = current_device();
+    if (dev < 0) return GQA_ERR_CUDA;
     if (dev >= kNoAllocMaxDevices) return GQA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    NoAllocDevice& d = g_noalloc_dev[dev];
-    if (!d.ready) {
-        void* a = nullptr;
-        void* s = nullptr;
-        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess) return GQA_ERR_CUDA;
-        if (cudaGetSymbolAddress(&s, g_noalloc_status) != cudaSuccess) return GQA_ERR_CUDA;
-        d.scratch = a;
-        d.status = static_cast<unsigned*>(s);
-        d.ready = true;
+    void* a = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || !a) return GQA_ERR_CUDA;
+        g_noalloc_addr[dev].store(a, std::memory_order_release);
     }
-    *scratch = d.scratch;
-    *status = d.status;
+    *scratch = a;
     return GQA_OK;
 }
 
@@ -1437,55 +1453,17 @@ extern "C" int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, con
     if (B == 0) return GQA_OK;
     int ns = num_splits;
     if (ns == 0) {
-        int dev = -1, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return GQA_ERR_CUDA;
+        const int sms = num_sms();
+        if (sms <= 0) return GQA_ERR_CUDA;
         ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
-    const int cs = cluster_size_for(ns, int64_t(ns) * H_kv * B);
-    const WsLayout wl = ws_layout(B, H_q, d, ns, cs);
+    const WsLayout wl = ws_layout(B, H_q, d, ns, cluster_size_for(ns, int64_t(ns) * H_kv * B));
     if (wl.total > kNoAllocScratchBytes) return GQA_ERR_WORKSPACE;
     void* scratch = nullptr;
-    unsigned* status = nullptr;
-    rc = noalloc_setup(&scratch, &status);
+    rc = noalloc_scratch(&scratch);
     if (rc != GQA_OK) return rc;
-    // The status word only ever has bits OR-ed in; start each call from zero.
-    if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return GQA_ERR_CUDA;
-
-    // The same launch sequence as gqa_attn_decode, with the fixed scratch and
-    // status word in place of the library-owned ones.
-    CUtensorMap maps[4];
-    const uint64_t outer = uint64_t(B) * H_kv;
-    if (gqa::encode_tmap_3d_bf16(&maps[0], k, d, S_max, outer, 64, kTileT,
-                                 CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
-        gqa::encode_tmap_3d_bf16(&maps[1], v, d, S_max, outer, 64, kTileT,
-                                 CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
-        return GQA_ERR_CUDA;
-    maps[2] = maps[0];  // unused by the bf16 kernels
-    maps[3] = maps[1];
-    SplitParams sp{};
-    sp.q = q;
-    sp.seqlens = seqlens;
-    sp.o = o;
-    sp.lse = lse;
-    uint8_t* w8 = static_cast<uint8_t*>(scratch);
-    const bool parts = wl.total > 0;
-    sp.part_o = parts ? reinterpret_cast<float*>(w8 + wl.o_off) : nullptr;
-    sp.part_m = parts ? reinterpret_cast<float*>(w8 + wl.m_off) : nullptr;
-    sp.part_l = parts ? reinterpret_cast<float*>(w8 + wl.l_off) : nullptr;
-    sp.status = status;
-    sp.B = B;
-    sp.H_q = H_q;
-    sp.H_kv = H_kv;
-    sp.G = H_q / H_kv;
-    sp.S_max = S_max;
-    sp.ns = ns;
-    sp.L = gqa::split_len(S_max, ns);
-    sp.n_groups = ns / cs;
-    sp.warm_l2 = int64_t(ns) * H_kv * B <= num_sms() ? 1 : 0;  // a single wave
-    sp.scale_log2 = scale * kLog2e;
-    return d == 128 ? launch<128, false>(sp, cs, maps, stream)
-                    : launch<64, false>(sp, cs, maps, stream);
+    // The same path as gqa_attn_decode_ws, with the fixed array as workspace.
+    return run(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, ns, scratch,
+               kNoAllocScratchBytes, stream);
 }

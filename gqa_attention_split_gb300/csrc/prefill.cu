@@ -68,6 +68,27 @@ struct Params {
     int inject_timeout;  // test hook: block 0 withholds its (first) Q copy
 };
 
+#ifdef GQA_DEBUG
+// Debug builds only: S = Q K^T tiles the MMA issuers actually issued, per
+// (batch, query head, query block, KV tile), split by the §5.4 class of the
+// tile (all past, partial, all future). A correct schedule issues no
+// all-future tile and exactly the all-past and partial ones.
+static __device__ unsigned long long g_dbg_tiles[3];
+
+__device__ __forceinline__ void dbg_count_tile(unsigned long long (&cnt)[3], const Params& p,
+                                               int qs, int qe, int j, int heads) {
+    const int ks = j * BN, ke = min(ks + BN, p.S_kv);
+    cnt[p.causal ? tile_class(qs, qe, ks, ke) : kTileAllPast] += heads;
+}
+__device__ __forceinline__ void dbg_flush_tiles(const unsigned long long (&cnt)[3]) {
+    for (int c = 0; c < 3; ++c)
+        if (cnt[c]) atomicAdd(&g_dbg_tiles[c], cnt[c]);
+}
+#define GQA_DBG(...) __VA_ARGS__
+#else
+#define GQA_DBG(...)
+#endif
+
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y,
                                          int z, uint32_t bar) {
     asm volatile(
@@ -201,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pdesc = tc::sdesc_sw128(psm, 16, 1024);
             const uint32_t qlo = uint32_t(qdesc), qhi = uint32_t(qdesc >> 32);
             const uint32_t plo = uint32_t(pdesc), phi = uint32_t(pdesc >> 32);
+            GQA_DBG(unsigned long long dbg[3] = {0, 0, 0};)
             bool alive = mbar_wait_bounded(bar(kQFull), 0, p.status);
             for (int j = 0; j <= n_tiles && alive; ++j) {
                 if (j < n_tiles) {
@@ -222,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ss_lo<1>(dst, qlo + off, qhi, klo + off, khi, idesc_s);
                     }
                     tc::commit(bar(kSFull + (j & 1)));
+                    GQA_DBG(dbg_count_tile(dbg, p, qs, qe, j, 1);)
                 }
                 if (j >= 1) {
                     const int jp = j - 1, s = jp % kStages;
@@ -245,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::commit(bar(kKVEmpty + s));
                 }
             }
+            GQA_DBG(dbg_flush_tiles(dbg);)
             // No MMA may still be running when the tensor memory is freed.
             tc::commit(bar(kMmaDrain));
             mbar_wait_bounded(bar(kMmaDrain), 0, p.status);
@@ -643,6 +667,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         bool alive = true;
         int r = 0;   // ring items consumed so far
         int tt = 0;  // KV tiles finished so far (S and P barrier phases)
+        GQA_DBG(unsigned long long dbg[3] = {0, 0, 0};)
         for (int it = 0; alive && pair_item(p, it, w); ++it) {
             const int n = w.n_tiles;
             alive = mbar_wait_bounded(bar(pQFull), it & 1, p.status) && wait_item(r);
@@ -650,6 +675,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             tc::fence_after_sync();
             issue_s(0, r);
             issue_s(1, r);
+            GQA_DBG(dbg_count_tile(dbg, p, w.qs, w.qe, 0, 2);)
             tc::commit(bar(pSlotEmpty + r % kRingSlots));  // K_0 read by both S MMAs
             if (n == 1) tc::commit(bar(pQEmpty));
             for (int j = 0; j < n && alive; ++j) {
@@ -670,6 +696,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     if (g == 1) tc::commit(bar(pSlotEmpty + rv % kRingSlots));  // done with V_j
                     if (more) {
                         issue_s(g, rv + 1);
+                        GQA_DBG(dbg_count_tile(dbg, p, w.qs, w.qe, j + 1, 1);)
                         if (g == 1) {
                             tc::commit(bar(pSlotEmpty + (rv + 1) % kRingSlots));  // K_{j+1}
                             if (j + 2 == n) tc::commit(bar(pQEmpty));  // last S of the item
@@ -682,6 +709,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             r += 2 * n;
             tt += n;
         }
+        GQA_DBG(dbg_flush_tiles(dbg);)
         // No MMA may still run when the tensor memory is freed.
         tc::commit(bar(pDrain));
         mbar_wait_bounded(bar(pDrain), 0, p.status);
@@ -870,7 +898,9 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
     if (!q || !k || !v || !o) return GQA_ERR_INVALID_ARG;
     if (B < 0 || B > 65535 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 1 || q_offset < 0)
         return GQA_ERR_INVALID_ARG;
-    if (H_q % H_kv != 0 || !isfinite(scale)) return GQA_ERR_INVALID_ARG;
+    // scale > 0: the kernels take each row's maximum over the raw scores and
+    // scale it, which is the maximum of the scaled scores only for scale > 0
+    if (H_q % H_kv != 0 || !isfinite(scale) || !(scale > 0.f)) return GQA_ERR_INVALID_ARG;
     if (causal && int64_t(q_offset) + T_q > S_kv) return GQA_ERR_INVALID_ARG;
     if (d != D) return GQA_ERR_UNSUPPORTED;
     if (int64_t(B) * H_q * T_q >= (int64_t(1) << 31) ||
@@ -919,15 +949,16 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     prm.n_mblocks = (T_q + BM - 1) / BM;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.inject_timeout = take_injected_timeout() ? 1 : 0;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static std::atomic<uint64_t> attr_done{0};  // once per device
+    const int dev = current_device();
+    if (device_attrs_pending(attr_done, dev)) {
         if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(prefill_pair_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairSmemBytes) != cudaSuccess)
             return GQA_ERR_CUDA;
-        attr_set = true;
+        device_attrs_mark(attr_done, dev);
     }
     // Even group sizes run two heads of a KV group per CTA; odd ones one head.
     const bool pair = prm.G % 2 == 0;
@@ -953,6 +984,27 @@ extern "C" int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint
                                 int causal, float scale, cudaStream_t stream) {
     return gqa_attn_prefill_ex(q, k, v, o, lse, B, 64, 8, 128, T_q, S_kv, q_offset, causal,
                                scale, stream);
+}
+
+extern "C" int gqa_attn_debug_tile_counts(int64_t* counts, int clear) {
+#ifdef GQA_DEBUG
+    if (!counts) return GQA_ERR_INVALID_ARG;
+    unsigned long long c[3] = {0, 0, 0};
+    if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(c, gqa::prefill::g_dbg_tiles, sizeof(c)) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    for (int i = 0; i < 3; ++i) counts[i] = int64_t(c[i]);
+    if (clear) {
+        const unsigned long long z[3] = {0, 0, 0};
+        if (cudaMemcpyToSymbol(gqa::prefill::g_dbg_tiles, z, sizeof(z)) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+#else
+    (void)counts;
+    (void)clear;
+    return GQA_ERR_UNSUPPORTED;
+#endif
 }
 
 #ifdef GQA_TRACE

@@ -7,25 +7,40 @@
 #include <atomic>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "gqa_attn.h"
 #include "ptx.cuh"
 #include "runtime.cuh"
 
 namespace gqa {
+
+// The device status word lives in this module's own device memory, one copy
+// per GPU, so reading or clearing it never allocates. Kernels receive its
+// device address as a parameter (host code only has a host-side stand-in for
+// the symbol, looked up per device below).
+static __device__ unsigned g_status_word;
+
 namespace {
 
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned*> g_status[kMaxDevices];  // device -> address of g_status_word
+std::atomic<int> g_sms[kMaxDevices];            // device -> SM count (0: not read yet)
 std::mutex g_mu;
-std::map<int, unsigned*> g_status;  // device -> status word
-std::map<int, int> g_sms;           // device -> SM count
 
 struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
+    // Buffers replaced by a larger one. They are never freed: a CUDA graph
+    // captured earlier on this stream may still use one. Each growth at least
+    // doubles the size, so together they stay below the current buffer.
+    std::vector<void*> retired;
 };
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+}  // namespace
 
 int current_device() {
     int dev = -1;
@@ -33,33 +48,36 @@ int current_device() {
     return dev;
 }
 
-}  // namespace
+bool device_attrs_pending(const std::atomic<uint64_t>& done, int dev) {
+    return dev < 0 || dev >= 64 || !(done.load(std::memory_order_acquire) & (uint64_t(1) << dev));
+}
+
+void device_attrs_mark(std::atomic<uint64_t>& done, int dev) {
+    if (dev >= 0 && dev < 64) done.fetch_or(uint64_t(1) << dev, std::memory_order_release);
+}
 
 unsigned* status_word() {
     const int dev = current_device();
-    if (dev < 0) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mu);
-    auto it = g_status.find(dev);
-    if (it != g_status.end()) return it->second;
-    unsigned* p = nullptr;
-    if (cudaMalloc(&p, sizeof(unsigned)) != cudaSuccess) return nullptr;
-    if (cudaMemset(p, 0, sizeof(unsigned)) != cudaSuccess) {
-        cudaFree(p);
-        return nullptr;
-    }
-    g_status[dev] = p;
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned* p = g_status[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_status_word) != cudaSuccess) return nullptr;
+    p = static_cast<unsigned*>(a);
+    g_status[dev].store(p, std::memory_order_release);
     return p;
 }
 
 int num_sms() {
     const int dev = current_device();
     if (dev < 0) return -1;
-    std::lock_guard<std::mutex> lock(g_mu);
-    auto it = g_sms.find(dev);
-    if (it != g_sms.end()) return it->second;
+    if (dev < kMaxDevices) {
+        const int n = g_sms[dev].load(std::memory_order_relaxed);
+        if (n > 0) return n;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    g_sms[dev] = n;
+    if (dev < kMaxDevices) g_sms[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -74,13 +92,9 @@ void* stream_workspace(cudaStream_t stream, size_t bytes) {
         return nullptr;
     // Grow by at least 2x so a sequence of growing calls allocates O(log) times.
     size_t want = bytes > 2 * w.bytes ? bytes : 2 * w.bytes;
-    if (w.ptr) {
-        if (cudaFreeAsync(w.ptr, stream) != cudaSuccess) return nullptr;
-        w.ptr = nullptr;
-        w.bytes = 0;
-    }
     void* p = nullptr;
     if (cudaMallocAsync(&p, want, stream) != cudaSuccess) return nullptr;
+    if (w.ptr) w.retired.push_back(w.ptr);
     w.ptr = p;
     w.bytes = want;
     return p;
@@ -166,7 +180,7 @@ extern "C" const char* gqa_attn_strerror(int code) {
     switch (code) {
         case GQA_OK: return "ok";
         case GQA_ERR_INVALID_ARG: return "invalid argument";
-        case GQA_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, G <= 8)";
+        case GQA_ERR_UNSUPPORTED: return "unsupported shape (decode: d 64 or 128 and G <= 8; prefill: d 128)";
         case GQA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
         case GQA_ERR_CUDA: return "CUDA runtime or driver error";
         case GQA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";

@@ -7,11 +7,25 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace gqa {
 
-// Device pointer to the status word of the current device (allocated and
-// zeroed on first use). Returns nullptr if that fails.
+// Device address of the status word of the current device: a variable in
+// this library's own device memory (zero at load; nothing is allocated),
+// looked up once per device. Returns nullptr if that fails.
 unsigned* status_word();
+
+// Current device ordinal, or -1.
+int current_device();
+
+// Per-device "launch attributes already set" flags, one bit per device in
+// `done`: function attributes such as the dynamic shared-memory limit apply
+// to the device current when they are set, so each device needs its own.
+// pending() is true until mark() ran for that device (always true for
+// ordinals >= 64, which then set the attributes on every launch).
+bool device_attrs_pending(const std::atomic<uint64_t>& done, int dev);
+void device_attrs_mark(std::atomic<uint64_t>& done, int dev);
 
 // Current device's SM count (cached), or a negative value on failure.
 int num_sms();
@@ -21,8 +35,9 @@ void set_injected_timeouts(int launches);
 bool take_injected_timeout();
 
 // Library-owned workspace of at least `bytes` for (current device, stream).
-// Grows with stream-ordered allocation; returns nullptr on failure or when
-// it would have to grow while `stream` is being captured.
+// Grows with stream-ordered allocation; a buffer it replaces is kept (never
+// freed) because work captured earlier may still use it. Returns nullptr on
+// failure or when it would have to grow while `stream` is being captured.
 void* stream_workspace(cudaStream_t stream, size_t bytes);
 
 // Encodes a 3-D bf16 tensor map over a [outer, rows, inner] row-major tensor

@@ -32,8 +32,10 @@
  * Errors: every entry point returns 0 (GQA_OK) or a negative code and checks
  * its arguments on the host before launching anything; an invalid argument
  * never reaches the GPU. Errors the device detects (a bounded wait that ran
- * out, a seqlen outside [0, S_max]) set a device status word that
- * gqa_attn_check() reads.
+ * out, a seqlen outside [0, S_max]) set the library's device status word (one
+ * per GPU, in the library's own device memory), which gqa_attn_check() reads
+ * and clears. Every entry point reports there, gqa_attn_decode_noalloc
+ * included.
  */
 #ifndef GQA_ATTN_H_
 #define GQA_ATTN_H_
@@ -51,7 +53,7 @@ typedef struct CUstream_st* cudaStream_t;
 enum {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = -1,    /* null pointer, bad size, H_q % H_kv != 0, ... */
-    GQA_ERR_UNSUPPORTED = -2,    /* d not in {64, 128}, or G > 8 */
+    GQA_ERR_UNSUPPORTED = -2,    /* decode: d not in {64, 128} or G > 8; prefill: d != 128 */
     GQA_ERR_MISALIGNED = -3,     /* a tensor pointer is not 16-byte aligned */
     GQA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
     GQA_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (device status) */
@@ -81,9 +83,13 @@ enum {
  *   scale      : softmax scale (finite), usually 1/sqrt(d).
  *   num_splits : 0 = automatic, else 1..8192.
  * The workspace for the per-split partials is library-owned: one buffer per
- * (device, stream), grown with stream-ordered allocation on first use. The
- * first call on a stream should therefore happen before any stream capture.
- * Calls on different streams never share a workspace.
+ * (device, stream), grown with stream-ordered allocation when a call needs
+ * more than it holds. A call that would have to grow it during stream capture
+ * returns GQA_ERR_WORKSPACE, so make the first (largest) call on a stream
+ * before capturing. A buffer replaced by a larger one is kept until the
+ * process exits (never freed), so work captured earlier on the stream, such
+ * as a CUDA graph, stays valid; the kept buffers together are smaller than the
+ * current one. Calls on different streams never share a workspace.
  */
 int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                     uint16_t* o, float* lse, const int32_t* seqlens,
@@ -126,8 +132,8 @@ size_t gqa_attn_decode_workspace_size(int B, int H_q, int d, int num_splits);
  *     before reading it). Calls that overlap on the GPU, on any streams, race
  *     on it: serialise them.
  *   - Device-detected errors (a clamped seqlen, a bounded wait that ran out)
- *     go to a status word in the same fixed area; gqa_attn_check() does not
- *     report them.
+ *     go to the library's status word like every other call's; read them
+ *     with gqa_attn_check(), which allocates nothing either.
  */
 #define GQA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -207,8 +213,11 @@ int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes, const uint8_t*
  * causal != 0: key j is visible to query t iff j <= q_offset + t; fully
  * future KV tiles are skipped and partial tiles masked (§5.4). causal == 0:
  * every key is visible. Fixed to the Llama3-70B head geometry of §0
- * (H_q = 64, H_kv = 8, d = 128); gqa_attn_prefill_ex takes any supported one.
- *   lse : [B, H_q, T_q] fp32, or NULL.
+ * (H_q = 64, H_kv = 8, d = 128); gqa_attn_prefill_ex takes any supported one
+ * (d = 128, any H_q divisible by H_kv).
+ *   lse   : [B, H_q, T_q] fp32, or NULL.
+ *   scale : softmax scale, finite and > 0 (§0.5 fixes 1/sqrt(d)); anything
+ *           else returns GQA_ERR_INVALID_ARG.
  */
 int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      uint16_t* o, float* lse,
@@ -269,8 +278,9 @@ int gqa_attn_prefill_block_n(void);
 /* ------------------------------------------------------------ status ----- */
 
 /* Synchronises `stream`, then reads and clears the device status word of the
- * current device. Returns GQA_OK, GQA_ERR_DEVICE_TIMEOUT,
- * GQA_ERR_DEVICE_BAD_INPUT or GQA_ERR_CUDA. */
+ * current device (allocates no memory). Returns GQA_OK,
+ * GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_DEVICE_BAD_INPUT or GQA_ERR_CUDA. The word
+ * collects the errors of every call on that device since the last check. */
 int gqa_attn_check(cudaStream_t stream);
 
 /* Test hook for failure reporting: the next `launches` decode or prefill
@@ -282,6 +292,17 @@ int gqa_attn_check(cudaStream_t stream);
  * such a call is undefined; nothing faults and later calls are unaffected.
  * 0 disarms. Returns GQA_OK or GQA_ERR_INVALID_ARG (launches < 0). */
 int gqa_attn_debug_inject_timeout(int launches);
+
+/* Causal-skip check (page: ADR-0060 §11, verification plan: the number of
+ * tile GEMMs equals the lower-triangle tile count). In a library built with
+ * -DGQA_DEBUG the prefill MMA issuers count every S = Q K^T tile they issue,
+ * per (batch row, query head, query block, KV tile), split by the §5.4 class
+ * of gqa_attn_tile_class (causal == 0: every tile counts as all past). This
+ * synchronises the device, writes counts[0..2] = all-past, partial,
+ * all-future tiles issued since the last clear, and zeroes the counters when
+ * clear != 0. A correct schedule issues no all-future tile. Other builds
+ * return GQA_ERR_UNSUPPORTED and touch nothing. */
+int gqa_attn_debug_tile_counts(int64_t* counts, int clear);
 
 /* Static, human-readable text for a return code. */
 const char* gqa_attn_strerror(int code);

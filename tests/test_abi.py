@@ -190,6 +190,16 @@ def test_decode_empty_batch_is_a_no_op(L):
     ((0, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 1, 0.1), api.GQA_ERR_INVALID_ARG),
     ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 7, 128, 128, 128, 0, 1, 0.1), api.GQA_ERR_INVALID_ARG),
     ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, -1, 1, 0.1), api.GQA_ERR_INVALID_ARG),
+    # the scale must be finite and > 0 (the kernels scale each row's raw maximum)
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 1, 0.0), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 1, -0.1), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 0, -0.1), api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 1, float("inf")),
+     api.GQA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 1, float("nan")),
+     api.GQA_ERR_INVALID_ARG),
+    # prefill runs d = 128 only
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 64, 128, 128, 0, 1, 0.1), api.GQA_ERR_UNSUPPORTED),
 ])
 def test_prefill_bad_args_return_codes_without_launch(L, args, code):
     assert api.gqa_attn_prefill_ex(*args, None) == code
@@ -222,3 +232,10 @@ def test_ring_append_bad_args_return_codes_without_launch(L, args, code):
 ])
 def test_decode_ring_bad_args_return_codes_without_launch(L, args, code):
     assert api.gqa_attn_decode_ring(*args, None) == code
+
+
+def test_debug_tile_counts_need_the_debug_build(L):
+    # the product library has no tile counters: the call reports that and
+    # touches nothing (no device work either)
+    rc, counts = api.gqa_attn_debug_tile_counts(clear=True)
+    assert rc == api.GQA_ERR_UNSUPPORTED and counts == [0, 0, 0]

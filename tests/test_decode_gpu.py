@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import oracle as orc
+from _fullsize import attention_by_group
 from gqa_attention_split_gb300 import api, build
 from gqa_attention_split_gb300 import workloads as wl
 
@@ -126,22 +127,16 @@ def test_llama70b_decode_8k_all_rows():
         assert_close(o2, lse2, O.reshape(1, w.H_q, w.d), L.reshape(1, w.H_q), f"8k ns={ns}")
 
 
-def test_ragged_long_context_sampled_groups():
+def test_ragged_long_context_every_row():
+    # All 4 x 64 query-head rows of the ragged 128K batch (every (row, KV head)
+    # group, padded cache masked by seqlens), against the fp64 oracle.
     w = wl.RAGGED_DECODE_128K
     q, k, v, sl = wl.decode_inputs(w)
     assert sl.min() >= 16384 and sl.max() <= 131072
     o, lse = run_decode(q, k, v, sl, 0)
-    o, lse = o.cpu(), lse.cpu()
-    G = w.H_q // w.H_kv
-    for b in range(w.B):
-        for kv in (0, w.H_kv - 1) if b % 2 == 0 else (3,):
-            n = int(sl[b])
-            Kf, Vf = orc.to_f64(k[b, kv, :n]), orc.to_f64(v[b, kv, :n])
-            qg = orc.to_f64(q[b, kv * G:(kv + 1) * G])
-            O, L = orc.attention(qg[None, :, None, :], Kf[None, None], Vf[None, None],
-                                 scale=w.scale)
-            assert_close(o[b, kv * G:(kv + 1) * G], lse[b, kv * G:(kv + 1) * G], O[0, :, 0],
-                         L[0, :, 0], f"ragged b={b} kv={kv} n={n}")
+    O, L = attention_by_group(q[:, :, None], k, v, scale=w.scale, seqlens=sl.tolist(),
+                              task_gb=3.0)
+    assert_close(o, lse, O[:, :, 0], L[:, :, 0], "ragged 128K")
 
 
 def test_deterministic_bitwise():
@@ -192,3 +187,35 @@ def test_out_of_range_seqlen_is_clamped_and_reported():
     api.check()  # the status word was cleared
     O, L = oracle_decode(q, k, v, torch.tensor([100, 0]), 1 / math.sqrt(64))
     assert_close(o, lse, O[:, :, 0], L[:, :, 0], "clamped")
+
+
+def test_graph_captured_before_workspace_growth_stays_valid():
+    # A CUDA graph captured on a stream keeps the workspace address it saw. A
+    # later call on that stream that needs a larger workspace gets a new
+    # buffer; the old one must stay allocated so the graph still replays
+    # correctly (the library keeps replaced buffers instead of freeing them).
+    st = torch.cuda.Stream()
+    q, k, v, sl = wl.small_decode(1, 16, 2, 128, 4000, seed=510, seqlens=[3999])
+    qd, kd, vd, sd = q.cuda(), k.cuda(), v.cuda(), sl.cuda()
+    o = torch.empty_like(qd)
+    lse = torch.empty((1, 16), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(st):
+        api.decode(qd, kd, vd, sd, num_splits=32, out=o, lse=lse)  # two clusters per row
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        api.decode(qd, kd, vd, sd, num_splits=32, out=o, lse=lse)
+    # a much larger problem on the same stream: the workspace grows
+    q2, k2, v2, sl2 = wl.small_decode(4, 64, 8, 128, 8192, seed=511)
+    with torch.cuda.stream(st):
+        api.decode(q2.cuda(), k2.cuda(), v2.cuda(), sl2.cuda(), num_splits=64)
+    st.synchronize()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        o.zero_()
+        lse.zero_()
+        g.replay()
+    st.synchronize()
+    api.check(st)
+    O, L = oracle_decode(q, k, v, sl, 1 / math.sqrt(128))
+    assert_close(o, lse, O[:, :, 0], L[:, :, 0], "graph replay after workspace growth")

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import oracle as orc
+from _fullsize import attention_by_group
 from gqa_attention_split_gb300 import api, build
 from gqa_attention_split_gb300 import workloads as wl
 
@@ -82,28 +83,84 @@ def test_a_later_tile_with_much_larger_scores(causal):
     O, L = orc.attention(q, k, v, scale=1 / math.sqrt(128), causal=causal)
     assert_close(o, lse, O, L, f"large scores causal={causal}")
 
-def _sample_rows(B, H_q, T_q, n, seed):
-    rng = np.random.default_rng(seed)
-    rows = {(0, 0, 0), (B - 1, H_q - 1, T_q - 1), (0, H_q // 2, min(127, T_q - 1)),
-            (0, 1, min(128, T_q - 1))}
-    while len(rows) < n:
-        rows.add((int(rng.integers(B)), int(rng.integers(H_q)), int(rng.integers(T_q))))
-    return sorted(rows)
-
-
 @pytest.mark.parametrize("w", [wl.CAUSAL_PREFILL_8K, wl.CHUNKED_PREFILL_32K],
                          ids=lambda w: w.name)
-def test_full_size_workloads_sampled_rows(w):
+def test_full_size_workloads_every_row(w):
+    # Every output row of the 8K causal prefill (2048 work items of the
+    # persistent kernel over the SMs) and of the chunked 32K prefill at
+    # q_offset 30720 (1024 items), against the fp64 oracle.
     q, k, v = wl.prefill_inputs(w)
     o, lse = run_prefill(q, k, v, w.q_offset, True)
-    rows = _sample_rows(w.B, w.H_q, w.T_q, 48, seed=w.seed)
-    O, L = orc.attention_rows(q, k, v, rows, scale=w.scale, causal=True, q_offset=w.q_offset)
-    og = np.stack([o[b, h, t] for b, h, t in rows])
-    lg = np.array([lse[b, h, t] for b, h, t in rows])
-    assert_close(og, lg, O, L, w.name)
-    # properties that hold at any size: finite everywhere, lse >= the log of the
-    # row's visible-key count lower bound is not fixed, but lse must be finite
+    O, L = attention_by_group(q, k, v, scale=w.scale, causal=True, q_offset=w.q_offset)
+    assert_close(o, lse, O, L, w.name)
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,off,causal", [
+    (1, 64, 8, 2048, 2048, 0, True),       # 512 items over at most 152 CTAs
+    (2, 64, 8, 1024, 4096, 3072, True),    # chunk at an offset, two batch rows: 512 items
+    (1, 64, 8, 1024, 1536, 0, False),      # full attention: 256 items
+    (1, 48, 8, 1536, 1536, 0, True),       # G = 6: pairs cross no KV group, 288 items
+    (1, 24, 8, 1100, 1300, 200, True),     # G = 3 (one head per CTA), ragged last block
+])
+def test_many_work_items_per_cta_every_row(B, H_q, H_kv, T_q, S_kv, off, causal):
+    # The persistent kernel runs several items per CTA here: barrier phases
+    # counted across items, Q reloaded once the previous item's last S MMAs
+    # completed, and PV(0) overwriting the previous item's O after its
+    # epilogue read it. Every row is compared.
+    q, k, v = wl.small_prefill(B, H_q, H_kv, 128, T_q, S_kv, off, seed=20 + T_q + S_kv + H_q)
+    o, lse = run_prefill(q, k, v, off, causal)
+    O, L = attention_by_group(q, k, v, scale=1 / math.sqrt(128), causal=causal, q_offset=off)
+    assert_close(o, lse, O, L, f"B={B} H={H_q}/{H_kv} T={T_q} S={S_kv} off={off} c={causal}")
+
+
+def p_rounding_bound(q, k, v, O, *, causal, q_offset):
+    """Per-element bound on |O_gpu - O| from the kernels' arithmetic: P is
+    rounded to bf16 (relative error <= 2^-9 per weight) before the P.V MMA and
+    O is normalised by the sum of the rounded weights, so O_gpu is a convex
+    combination of the visible V rows whose weights differ from the exact ones
+    by a factor (1 + d_j) / (1 + mean d), |d_j| <= 2^-9. To first order
+    |dO_c| <= 2^-8 * max_j |v_jc - O_c| over the visible keys j, plus the
+    output's own bf16 rounding, 2^-9 |O_c|, plus 1e-4 for the fp32 sums."""
+    v = orc.to_f64(v)
+    G = q.shape[1] // k.shape[1]
+    v_rep = np.repeat(v, G, axis=1)                      # [B, H_q, S, d]
+    vmax = np.maximum.accumulate(v_rep, axis=2)          # prefix max / min over keys
+    vmin = np.minimum.accumulate(v_rep, axis=2)
+    T_q, S = q.shape[2], k.shape[2]
+    last = [(min(S, q_offset + t + 1) if causal else S) - 1 for t in range(T_q)]
+    hi, lo = vmax[:, :, last], vmin[:, :, last]          # [B, H_q, T_q, d]
+    spread = np.maximum(np.abs(hi - O), np.abs(lo - O))
+    return 2.0 ** -8 * spread + 2.0 ** -9 * np.abs(O) + 1e-4
+
+
+@pytest.mark.parametrize("scale", [0.05, 0.3])
+@pytest.mark.parametrize("causal", [True, False])
+def test_scales_other_than_one_over_sqrt_d(scale, causal):
+    # Any finite scale > 0 is accepted. 0.05 flattens the scores and meets the
+    # decode/prefill tolerance. 0.3 makes them ~3.4x sharper than 1/sqrt(128),
+    # with many lazy rescales; the weight of a few keys then dominates each row
+    # and their bf16 rounding no longer averages out, so the bar there is the
+    # bound the arithmetic fixes (p_rounding_bound), element by element.
+    B, H_q, H_kv, T, S, off = 1, 16, 2, 700, 900, 200
+    off = off if causal else 0
+    q, k, v = wl.small_prefill(B, H_q, H_kv, 128, T, S, off, seed=81)
+    o, lse = run_prefill(q, k, v, off, causal, scale=scale)
+    O, L = orc.attention(q, k, v, scale=scale, causal=causal, q_offset=off)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+    err = np.abs(o - O)
+    bound = p_rounding_bound(q, k, v, O, causal=causal, q_offset=off)
+    assert (err <= bound).all(), f"scale={scale}: max excess {(err - bound).max():.3e}"
+    assert np.abs(lse - L).max() <= LSE_ABS
+    if scale <= 1 / math.sqrt(128):
+        assert_close(o, lse, O, L, f"scale={scale} causal={causal}")
+
+
+def test_non_positive_scale_is_rejected():
+    q, k, v = wl.small_prefill(1, 8, 2, 128, 64, 64, 0, seed=82)
+    for bad in (0.0, -0.088):
+        with pytest.raises(api.GqaError) as e:
+            api.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=bad)
+        assert e.value.code == api.GQA_ERR_INVALID_ARG
 
 
 def test_deterministic_bitwise():

@@ -9,12 +9,14 @@ tolerance: max |dO| <= 1e-2, mean |dO| <= 1e-3, |d lse| <= 1e-3.
 """
 
 import math
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
 import torch
 
 import oracle as orc
+from _fullsize import workers
 from gqa_attention_split_gb300 import api, build
 from gqa_attention_split_gb300 import workloads as wl
 
@@ -120,7 +122,10 @@ def test_full_size_8k_decode_through_the_gpu_quantiser():
     assert np.abs(O - O16[:, :, 0]).max() < 0.05
 
 
-def test_ragged_128k_sampled_heads():
+def test_ragged_128k_every_head():
+    # All 4 x 64 query-head rows of the ragged 128K batch over the GPU
+    # quantiser's cache, against attention over the oracle's dequantised
+    # cache (the codes are compared bit for bit on one group first).
     w = wl.RAGGED_DECODE_128K
     q, k, v, sl = wl.decode_inputs(w)
     kc, vc, ks, vs = api.quantize_kv_q8(k.cuda(), v.cuda())
@@ -128,15 +133,49 @@ def test_ragged_128k_sampled_heads():
     api.check()
     o, lse = o.cpu(), lse.cpu()
     G = w.H_q // w.H_kv
-    rng = np.random.default_rng(5)
-    for b in range(w.B):
-        for h in rng.choice(w.H_q, size=3, replace=False):
-            kv = h // G
-            n = int(sl[b])
-            kcb, ksb = orc.quantize_q8(k[b:b + 1, kv:kv + 1, :n])
-            vcb, vsb = orc.quantize_q8(v[b:b + 1, kv:kv + 1, :n])
-            O, L = orc.attention_q8(q[b:b + 1, h:h + 1], kcb, ksb, vcb, vsb, scale=w.scale)
-            _assert_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O, L, f"b={b} h={h}")
+    n0 = int(sl[0])
+    kc0, ks0 = orc.quantize_q8(k[0:1, 0:1, :n0])
+    assert np.array_equal(kc[0:1, 0:1, :n0].cpu().numpy(), _stored(kc0))
+    assert np.array_equal(ks[0:1, 0:1, :n0].cpu().numpy(), ks0)
+    del kc, vc, ks, vs
+
+    def group(bk):
+        b, kv = bk
+        n = int(sl[b])
+        kcb, ksb = orc.quantize_q8(k[b:b + 1, kv:kv + 1, :n])
+        vcb, vsb = orc.quantize_q8(v[b:b + 1, kv:kv + 1, :n])
+        return bk, orc.attention_q8(q[b:b + 1, kv * G:(kv + 1) * G], kcb, ksb, vcb, vsb,
+                                    scale=w.scale)
+
+    with ThreadPoolExecutor(workers(3.0)) as ex:
+        for (b, kv), (O, L) in ex.map(group, [(b, kv) for b in range(w.B)
+                                              for kv in range(w.H_kv)]):
+            _assert_close(o[b:b + 1, kv * G:(kv + 1) * G], lse[b:b + 1, kv * G:(kv + 1) * G],
+                          O, L, f"b={b} kv={kv}")
+
+
+@pytest.mark.parametrize("e", [16, -20])
+def test_query_magnitudes_outside_the_f16_range(e):
+    # The kernel runs its MMAs in f16. q * 2^16 has entries beyond f16's
+    # largest value (65504) and q * 2^-20 entries in f16's subnormals; with the
+    # scale divided by the same power of two the scores are those of q itself,
+    # so the result must match the oracle on (q * 2^e, scale * 2^-e).
+    S_max, G, H_kv, d = 1024, 8, 2, 128
+    lens = [1024, 700, 1]
+    q, k, v, _ = wl.small_decode(len(lens), G * H_kv, H_kv, d, S_max, seed=930)
+    qs = (q.float() * 2.0 ** e).to(torch.bfloat16)
+    assert torch.equal(qs.float(), q.float() * 2.0 ** e)  # exact power-of-two scaling
+    if e > 0:
+        assert qs.float().abs().max() > 65504
+    scale = 2.0 ** -e / math.sqrt(d)
+    kc, ks, vc, vs, dkc, dvc, dks, dvs = _oracle_cache(k, v)
+    O, L = orc.attention_q8(qs, kc, ks, vc, vs, scale=scale, seqlens=lens)
+    for ns in (1, 4):
+        o, lse = api.decode_q8(qs.cuda(), dkc, dvc, dks, dvs,
+                               torch.tensor(lens, dtype=torch.int32).cuda(), num_splits=ns,
+                               scale=scale)
+        api.check()
+        _assert_close(o, lse, O, L, f"q x 2^{e} ns={ns}")
 
 
 def test_decode_rejects_unsupported_shapes():

@@ -5,9 +5,11 @@ start-up, a host with its own allocator, a path that cannot take cudaMalloc's
 implicit synchronisation). This entry point keeps its scratch in a fixed array
 inside the library instead. The test calls it through the C ABI twice in a
 row, on different problems that both need scratch, and checks each result
-against gqa_attn_decode on the same inputs within the decode tolerance. This
-file is collected last so that a run stopping at the first failure has
-already run every other test.
+against gqa_attn_decode on the same inputs within the decode tolerance. Its
+device-side errors (a bounded wait that ran out, a clamped seqlen) reach the
+caller through gqa_attn_check(), which allocates nothing either. This file is
+collected last so that a run stopping at the first failure has already run
+every other test.
 """
 
 import math
@@ -54,7 +56,9 @@ def _assert_within_tolerance(ref, got):
     d_o = (o.float() - o_ref.float()).abs()
     assert torch.isfinite(o.float()).all()
     assert d_o.max().item() <= MAX_ABS and d_o.mean().item() <= MEAN_ABS
-    assert (l - l_ref).abs().max().item() <= LSE_ABS
+    fin = torch.isfinite(l_ref)
+    assert torch.equal(torch.isneginf(l), ~fin)  # empty rows: lse = -inf on both
+    assert (l[fin] - l_ref[fin]).abs().max().item() <= LSE_ABS
 
 
 def test_noalloc_matches_decode_on_two_calls_in_a_row():
@@ -76,3 +80,43 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = api.gqa_attn_decode_noalloc(fake, fake, fake, fake, None, None, B, H_q, 8, d, 65536,
                                      0.088, ns, None)
     assert rc == api.GQA_ERR_WORKSPACE
+
+
+def _noalloc(q, k, v, sl, o, lse, B, H_q, H_kv, d, S_max, ns):
+    rc = api.gqa_attn_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), sl.data_ptr(), B, H_q, H_kv, d, S_max,
+                                     1.0 / math.sqrt(d), ns,
+                                     torch.cuda.current_stream().cuda_stream)
+    assert rc == api.GQA_OK, api.strerror(rc)
+
+
+def test_noalloc_device_errors_reach_check():
+    B, H_q, H_kv, d, S_max, ns = 2, 8, 1, 128, 4096, 32  # two 16-split clusters per row
+    q, k, v, sl = wl.small_decode(B, H_q, H_kv, d, S_max, seed=903, seqlens=[4096, 2500])
+    q, k, v, sl = q.cuda(), k.cuda(), v.cuda(), sl.cuda()
+    o = torch.empty((B, H_q, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H_q), dtype=torch.float32, device="cuda")
+    api.check()  # start from a clear status word
+    # 1) the first block withholds one copy: its bounded wait runs out (~1 s)
+    assert api.gqa_attn_debug_inject_timeout(1) == api.GQA_OK
+    _noalloc(q, k, v, sl, o, lse, B, H_q, H_kv, d, S_max, ns)
+    with pytest.raises(api.GqaError) as e:
+        api.check()
+    assert e.value.code == api.GQA_ERR_DEVICE_TIMEOUT
+    # the next call is correct and reports nothing
+    _noalloc(q, k, v, sl, o, lse, B, H_q, H_kv, d, S_max, ns)
+    api.check()
+    ref = api.decode(q, k, v, sl, num_splits=ns)
+    api.check()
+    _assert_within_tolerance(ref, (o, lse))
+    # 2) a seqlen outside [0, S_max] is clamped and reported
+    bad = torch.tensor([S_max + 100, -3], dtype=torch.int32, device="cuda")
+    _noalloc(q, k, v, bad, o, lse, B, H_q, H_kv, d, S_max, ns)
+    with pytest.raises(api.GqaError) as e:
+        api.check()
+    assert e.value.code == api.GQA_ERR_DEVICE_BAD_INPUT
+    api.check()  # cleared by the read
+    ref = api.decode(q, k, v, torch.tensor([S_max, 0], dtype=torch.int32, device="cuda"),
+                     num_splits=ns)
+    api.check()
+    _assert_within_tolerance(ref, (o, lse))
