@@ -146,24 +146,41 @@ class ClockSampler:
 # --------------------------------------------------------------- CPU oracle
 
 
-def cpu_oracle_sample(seconds: float, steps: int = 1):
-    """Times the fp64 oracle, as it stands, on rows of the two workloads (one thread).
+def cpu_oracle_sample(seconds: float, steps: int = 1, procs: int = 1):
+    """Times the fp64 oracle, as it stands, on rows of the two workloads.
 
-    Runs in a fresh single-threaded process; each of `steps` samples spends about
-    `seconds` of CPU time. Returns one dict per step with decode GB/s (KV bytes of
-    whole decode calls, pro rata per query head) and prefill TFLOPS.
+    Runs `procs` fresh single-threaded worker processes side by side (each on
+    its own rows); each of `steps` samples spends about `seconds` of CPU time
+    per process. Returns one dict per step with decode GB/s (KV bytes of whole
+    decode calls, pro rata per query head) and prefill TFLOPS over all
+    processes (rows summed, the slowest process's time), and the process count.
     """
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(seconds),
-           "--cpu-worker-steps", str(steps)]
-    out = subprocess.run(cmd, env=env, capture_output=True, text=True,
-                         timeout=120 + 3 * seconds * steps)
-    if out.returncode != 0:
-        raise RuntimeError(out.stderr[-2000:])
-    return json.loads(out.stdout.strip().splitlines()[-1])
+    running = [subprocess.Popen(
+        [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(seconds),
+         "--cpu-worker-steps", str(steps), "--cpu-worker-offset", str(i)],
+        env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+        for i in range(procs)]
+    per_proc = []
+    for pr in running:
+        out, err = pr.communicate(timeout=300 + 3 * seconds * steps)
+        if pr.returncode != 0:
+            raise RuntimeError(err[-2000:])
+        per_proc.append(json.loads(out.strip().splitlines()[-1]))
+    res = []
+    for st in range(steps):
+        xs = [pp[st] for pp in per_proc]
+        dec_s = max(x["decode_s"] for x in xs)
+        pre_s = max(x["prefill_s"] for x in xs)
+        res.append({"decode_gbs": sum(x["decode_bytes"] for x in xs) / dec_s / 1e9,
+                    "decode_rows": sum(x["decode_rows"] for x in xs), "decode_s": dec_s,
+                    "prefill_tflops": sum(x["prefill_flops"] for x in xs) / pre_s / 1e12,
+                    "prefill_rows": sum(x["prefill_rows"] for x in xs), "prefill_s": pre_s,
+                    "threads": procs})
+    return res
 
 
-def cpu_worker(seconds: float, steps: int):
+def cpu_worker(seconds: float, steps: int, offset: int = 0):
     import torch
 
     torch.set_num_threads(1)
@@ -181,7 +198,8 @@ def cpu_worker(seconds: float, steps: int):
         t0 = time.perf_counter()
         r0 = rows
         while time.perf_counter() - t0 < seconds / 2 or rows == r0:
-            oracle.attention_rows(q[:, :, None], k, v, [(0, rows % w.H_q, 0)], scale=w.scale,
+            h = (rows + 7 * offset) % w.H_q
+            oracle.attention_rows(q[:, :, None], k, v, [(0, h, 0)], scale=w.scale,
                                   seqlens=sl.tolist())
             rows += 1
         td = time.perf_counter() - t0
@@ -189,17 +207,39 @@ def cpu_worker(seconds: float, steps: int):
         flops = 0.0
         n0 = n
         while time.perf_counter() - t0 < seconds / 2 or n == n0:
-            t = (n * 997) % p.T_q  # spread over the causal triangle
-            oracle.attention_rows(qp, kp, vp, [(0, (n * 13) % p.H_q, t)], scale=p.scale,
+            m = n + 131 * offset
+            t = (m * 997) % p.T_q  # spread over the causal triangle
+            oracle.attention_rows(qp, kp, vp, [(0, (m * 13) % p.H_q, t)], scale=p.scale,
                                   causal=True, q_offset=p.q_offset)
             flops += 4.0 * p.d * min(p.S_kv, p.q_offset + t + 1)
             n += 1
         tp = time.perf_counter() - t0
-        res.append({"decode_gbs": kv_bytes * (rows - r0) / w.H_q / td / 1e9,
-                    "decode_rows": rows - r0, "decode_s": td,
-                    "prefill_tflops": flops / tp / 1e12, "prefill_rows": n - n0,
-                    "prefill_s": tp, "threads": 1})
+        res.append({"decode_bytes": kv_bytes * (rows - r0) / w.H_q, "decode_rows": rows - r0,
+                    "decode_s": td, "prefill_flops": flops, "prefill_rows": n - n0,
+                    "prefill_s": tp})
     print(json.dumps(res))
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def bench_config(world: int) -> dict:
+    """The workload both arms run (the reference arm prints the same dict)."""
+    from gqa_attention_split_gb300 import workloads as wl
+
+    w, p = wl.LLAMA70B_DECODE_8K, wl.CAUSAL_PREFILL_8K
+    return {"workload": f"{LAYERS} x {w.name} decode (graph) + {p.name}",
+            "decode": {"B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d, "S_kv": w.S_max,
+                       "layers": LAYERS},
+            "prefill": {"B": p.B, "H_q": p.H_q, "H_kv": p.H_kv, "d": p.d, "T_q": p.T_q,
+                        "S_kv": p.S_kv, "causal": True},
+            "l2": "inputs larger than L2: 80 distinct 33.5 MB KV caches per step; "
+                  "prefill operands 335 MB",
+            "parallelism": f"replicas x{world}"}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -333,6 +373,29 @@ def run_ours(args, rank, world, local_rank):
     api.check(stream)
     plain_call_us = pl0.elapsed_time(pl1) * 1e3 / (3 * LAYERS)
 
+    # one decode call alone, L2 flushed before it (a 256 MB write), as a decode
+    # step whose neighbours are not attention calls sees it. A GPU-side sleep
+    # (~100 us) ahead of the start event keeps the host's launch work for the
+    # call out of the timed interval; no other kernel overlaps the call.
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    lone = []
+    with torch.cuda.stream(stream):
+        for i in range(23):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            stream.synchronize()
+            torch.cuda._sleep(200_000)
+            e0.record(stream)
+            api.decode(qs[i % LAYERS], ks[i % LAYERS], vs[i % LAYERS], seqlens, num_splits=ns,
+                       out=os_[0], lse=lses[0])
+            e1.record(stream)
+            stream.synchronize()
+            if i >= 3:
+                lone.append(e0.elapsed_time(e1) * 1e3)
+    api.check(stream)
+    del flush
+    lone_call_us = statistics.median(lone)
+
     dec_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
     pre_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
     dec_ms, pre_ms, tot_ms = aggregate_max([dec_ms, pre_ms, dec_ms + pre_ms], dev, world)
@@ -362,19 +425,17 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": tot_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic N(0,1) bf16, seeded; random KV caches (no trained weights)",
-        "config": {"workload": f"{LAYERS} x {w.name} decode (graph) + {p.name}",
-                   "decode": {"B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
-                              "S_kv": w.S_max, "layers": LAYERS, "num_splits": ns,
-                              "active_splits": splits_active},
-                   "prefill": {"B": p.B, "H_q": p.H_q, "H_kv": p.H_kv, "d": p.d,
-                               "T_q": p.T_q, "S_kv": p.S_kv, "causal": True},
-                   "l2": "inputs larger than L2: 80 distinct 33.5 MB KV caches per step; "
-                         "prefill operands 335 MB",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(world),
         "decode": {"kv_GBps": value, "pct_of_8TBps": 100 * dec_gbs_rank / NOMINAL_HBM_GBS,
                    "pct_of_measured_hbm": 100 * dec_gbs_rank / hbm_peak,
                    "us_per_layer_call": dec_call_s * 1e6,
+                   "num_splits": ns, "active_splits": splits_active,
                    "plain_loop_us_per_layer_call": plain_call_us,
+                   "lone_call_us": lone_call_us,
+                   "lone_call_GBps": kv_b / lone_call_us / 1e3,
+                   "lone_call_note": "one call alone after an L2 flush (host launch work "
+                                     "hidden behind a GPU sleep), median of 20; the graph "
+                                     "figure overlaps consecutive calls",
                    "tok_per_s_one_layer": w.B / dec_call_s,
                    "tok_per_s_80_layers": w.B / (dec_call_s * LAYERS)},
         "prefill": None if not have_prefill else {
@@ -475,29 +536,31 @@ def run_e2e(api, torch, dev, stream, w, ns, p, have_prefill, args, world):
 
 
 def run_reference(args, rank, world):
-    """The fp64 CPU oracle as the reference arm, on this arm's config and metric."""
+    """The fp64 CPU oracle as the reference arm, on this arm's config and metric,
+    on every host core (one single-threaded process per core, own rows each)."""
     if rank != 0:
         return None
-    # The whole run stays within a few minutes: about 150 s of CPU work in total.
+    # The whole run stays within a few minutes: about 150 s of CPU work per core.
     per = max(0.2, min(args.ref_seconds, 150.0 / (args.warmup + args.steps)))
-    per_step = cpu_oracle_sample(per, args.warmup + args.steps)
+    procs = host_cores()
+    per_step = cpu_oracle_sample(per, args.warmup + args.steps, procs=procs)
     timed = per_step[args.warmup:]
     info = timed[-1]
     dec = statistics.mean(x["decode_gbs"] for x in timed)
     pre = statistics.mean(x["prefill_tflops"] for x in timed)
     sample = (f"per step: {info['decode_rows']} query-head rows of the 8K decode "
               f"({info['decode_s']:.1f}s) and {info['prefill_rows']} rows of the 8K causal "
-              f"prefill ({info['prefill_s']:.1f}s), fp64 oracle, 1 thread")
+              f"prefill ({info['prefill_s']:.1f}s), fp64 oracle, {procs} single-threaded "
+              "processes")
     return {"impl": "reference", "metric": METRIC, "value": dec, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.mean(x["decode_s"] + x["prefill_s"] for x in timed),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic N(0,1) bf16 widened to fp64, seeded",
-            "config": {"workload": f"{LAYERS} x llama70b_decode_b1_s8192 decode (graph) + "
-                                   "llama70b_causal_prefill_b1_t8192"},
+            "config": bench_config(world),
             "prefill": {"TFLOPS": pre},
-            "cpu_baseline": {"value": dec, "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(),
-                             "kind": "oracle",
+            "cpu_baseline": {"value": dec, "unit": "GB/s", "cores": procs,
+                             "host_cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": dec, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -661,9 +724,10 @@ def main():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-worker-steps", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-worker-offset", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_worker is not None:
-        cpu_worker(args.cpu_worker, args.cpu_worker_steps)
+        cpu_worker(args.cpu_worker, args.cpu_worker_steps, args.cpu_worker_offset)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -687,14 +751,23 @@ def main():
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            cb = cpu_oracle_sample(args.cpu_seconds)[0]
+            # the oracle on every host core (one single-threaded process each),
+            # and on one thread
+            procs = host_cores()
+            cb = cpu_oracle_sample(args.cpu_seconds, procs=procs)[0]
+            c1 = cpu_oracle_sample(args.cpu_seconds)[0]
             res["cpu_baseline"] = {
-                "value": cb["decode_gbs"], "unit": "GB/s", "cores": cb["threads"],
+                "value": cb["decode_gbs"], "unit": "GB/s", "cores": procs,
                 "host_cores": os.cpu_count(), "kind": "oracle",
                 "sample": f"{cb['decode_rows']} query-head rows of the 8K decode in "
-                          f"{cb['decode_s']:.1f}s (fp64 oracle, 1 thread); prefill rows: "
-                          f"{cb['prefill_tflops']:.2e} TFLOP/s over {cb['prefill_rows']} rows",
-                "prefill_TFLOPS": cb["prefill_tflops"]}
+                          f"{cb['decode_s']:.1f}s on {procs} single-threaded processes (fp64 "
+                          f"oracle, own rows each); prefill: {cb['prefill_rows']} rows",
+                "prefill_TFLOPS": cb["prefill_tflops"],
+                "single_thread": {"value": c1["decode_gbs"], "unit": "GB/s",
+                                  "prefill_TFLOPS": c1["prefill_tflops"],
+                                  "sample": f"{c1['decode_rows']} decode rows in "
+                                            f"{c1['decode_s']:.1f}s, {c1['prefill_rows']} "
+                                            "prefill rows, 1 thread"}}
         else:
             res["cpu_baseline"] = None
         print(json.dumps(res), flush=True)

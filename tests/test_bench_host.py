@@ -80,8 +80,19 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cores"] == bench.host_cores()  # one process per host core
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    # the same workload description as the GPU arm prints
+    assert d["config"] == bench.bench_config(1)
+
+
+def test_cpu_sample_sums_rows_over_processes():
+    one = bench.cpu_oracle_sample(0.4, steps=1, procs=1)[0]
+    two = bench.cpu_oracle_sample(0.4, steps=1, procs=2)[0]
+    assert one["threads"] == 1 and two["threads"] == 2
+    assert two["decode_rows"] >= 2 and two["prefill_rows"] >= 2
+    assert one["decode_gbs"] > 0 and two["decode_gbs"] > 0
 
 
 def test_reference_arm_other_ranks_print_nothing():
