@@ -38,6 +38,9 @@ _SIGNATURES = {
                                 _P]),
     "gqa_attn_decode_workspace_size": (_S, [_I, _I, _I, _I]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "gqa_attn_decode_partial": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
+                                     _P]),
+    "gqa_attn_merge": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "gqa_attn_ring_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gqa_attn_quantize_kv_q8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "gqa_attn_decode_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -262,6 +265,66 @@ def decode(q, k, v, seqlens=None, *, num_splits: int = 0, scale: float | None = 
                                 _ptr(workspace), workspace.numel(), st)
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_attn_decode")
+    return out, lse
+
+
+def gqa_attn_decode_partial(q, k, v, o_part, lse_part, seqlens, B, H_q, H_kv, d, S_max, scale,
+                            num_splits, stream):
+    return lib().gqa_attn_decode_partial(q, k, v, o_part, lse_part, seqlens, B, H_q, H_kv, d,
+                                         S_max, scale, num_splits, stream)
+
+
+def gqa_attn_merge(o_parts, lse_parts, o, lse, R, rows, d, stream):
+    return lib().gqa_attn_merge(o_parts, lse_parts, o, lse, R, rows, d, stream)
+
+
+def decode_partial(q, k, v, seqlens=None, *, num_splits: int = 0, scale: float | None = None,
+                   out=None, lse=None, stream=None):
+    """Decode over one key slice with fp32 output for ``merge``: q [B,H_q,d],
+    k/v [B,H_kv,S_slice,d] bf16 CUDA. Returns (o fp32 [B,H_q,d], lse [B,H_q])."""
+    import torch
+
+    _check_cuda_bf16("q", q, 3)
+    _check_cuda_bf16("k", k, 4)
+    _check_cuda_bf16("v", v, 4)
+    B, H_q, d = q.shape
+    H_kv, S_max = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H_kv, S, d] matching q")
+    if seqlens is not None and (seqlens.dtype != torch.int32 or not seqlens.is_cuda
+                                or seqlens.numel() != B):
+        raise TypeError("seqlens must be an int32 CUDA tensor of B elements")
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = gqa_attn_decode_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seqlens),
+                                 B, H_q, H_kv, d, S_max, sc, num_splits, _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_decode_partial")
+    return out, lse
+
+
+def merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):
+    """Log-sum-exp merge of R partials: o_parts fp32 [R, ..., d], lse_parts
+    fp32 [R, ...] (CUDA, contiguous). Returns (o bf16 [..., d], lse [...])."""
+    import torch
+
+    if (o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32 or not o_parts.is_cuda
+            or not o_parts.is_contiguous() or not lse_parts.is_contiguous()
+            or tuple(o_parts.shape[:-1]) != tuple(lse_parts.shape)):
+        raise ValueError("o_parts [R, ..., d] and lse_parts [R, ...] must be contiguous fp32 CUDA")
+    R, d = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel()
+    if out is None:
+        out = torch.empty(tuple(o_parts.shape[1:]), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(tuple(lse_parts.shape[1:]), dtype=torch.float32, device=o_parts.device)
+    rc = gqa_attn_merge(_ptr(o_parts), _ptr(lse_parts), _ptr(out), _ptr(lse), R, rows, d,
+                        _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_merge")
     return out, lse
 
 

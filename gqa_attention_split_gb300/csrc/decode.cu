@@ -65,6 +65,7 @@ struct SplitParams {
     const uint16_t* q;        // [B, H_q, D]
     const int32_t* seqlens;   // [B] or null
     uint16_t* o;              // [B, H_q, D]   (written when n_groups == 1)
+    float* o32;               // [B, H_q, D] fp32 instead of o (partial decode), or null
     float* lse;               // [B, H_q] or null
     float* part_o;            // [B, H_q, n_groups, D]  unnormalised group partials
     float* part_m;            // [B, H_q, n_groups]     base-2 running max
@@ -155,7 +156,10 @@ __device__ __forceinline__ float warp_sum(float x) {
 __device__ __forceinline__ void emit(const SplitParams& p, size_t row, int gi, int dim, int D,
                                      float m, float l, float o) {
     if (p.n_groups == 1) {
-        p.o[row * D + dim] = to_bf16_bits(l > 0.f ? o / l : 0.f);
+        if (p.o32)
+            p.o32[row * D + dim] = l > 0.f ? o / l : 0.f;
+        else
+            p.o[row * D + dim] = to_bf16_bits(l > 0.f ? o / l : 0.f);
         if (dim == 0 && p.lse) p.lse[row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     } else {
         const size_t pr = row * p.n_groups + gi;
@@ -816,6 +820,7 @@ struct CombineParams {
     const float* part_l;
     const int32_t* seqlens;
     uint16_t* o;
+    float* o32;  // fp32 output instead of o (partial decode), or null
     float* lse;
     int B, H_q, S_max, n_groups;
     int64_t group_len;  // keys per group: cluster size * L
@@ -846,10 +851,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     seqlen = seqlen < 0 ? 0 : (seqlen > p.S_max ? p.S_max : seqlen);
     const int n_act = int((seqlen + p.group_len - 1) / p.group_len);
     float* out_lse = p.lse ? p.lse + row : nullptr;
-    uint16_t* out = p.o + size_t(row) * D + lane * kPer;
+    uint16_t* out = p.o32 ? nullptr : p.o + size_t(row) * D + lane * kPer;
+    float* out32 = p.o32 ? p.o32 + size_t(row) * D + lane * kPer : nullptr;
     if (n_act == 0) {
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) out[j] = 0;
+        for (int j = 0; j < kPer; ++j) {
+            if (out32)
+                out32[j] = 0.f;
+            else
+                out[j] = 0;
+        }
         if (lane == 0 && out_lse) *out_lse = -INFINITY;
         return;
     }
@@ -890,7 +901,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     const float lsum = warp_sum(lpart);
     const float inv = 1.f / lsum;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) out[j] = to_bf16_bits(acc[j] * inv);
+    for (int j = 0; j < kPer; ++j) {
+        if (out32)
+            out32[j] = acc[j] * inv;
+        else
+            out[j] = to_bf16_bits(acc[j] * inv);
+    }
     if (lane == 0 && out_lse) *out_lse = (mx + __log2f(lsum)) * kLn2;
     if (threadIdx.x == 0) GQA_TRACE_STAMP(kTraceCombineBase + blockIdx.x, 2);
 }
@@ -1011,7 +1027,7 @@ int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStre
             return GQA_ERR_CUDA;
         device_attrs_mark(attr_done, dev);
     }
-    CombineParams cp{sp.part_o, sp.part_m, sp.part_l, sp.seqlens, sp.o, sp.lse,
+    CombineParams cp{sp.part_o, sp.part_m, sp.part_l, sp.seqlens, sp.o, sp.o32, sp.lse,
                      sp.B, sp.H_q, sp.S_max, sp.n_groups, int64_t(cs) * sp.L};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((sp.B * sp.H_q + kCombineWarps - 1) / kCombineWarps);
@@ -1047,7 +1063,8 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
 int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse,
         const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max, float scale,
         int ns, void* ws, size_t ws_bytes, cudaStream_t stream, bool ring = false,
-        const float* k_scales = nullptr, const float* v_scales = nullptr) {
+        const float* k_scales = nullptr, const float* v_scales = nullptr,
+        float* o32 = nullptr) {
     const bool q8 = k_scales != nullptr;  // k, v are then int8 K codes and dim-major V codes
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
@@ -1090,6 +1107,7 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.q = q;
     sp.seqlens = seqlens;
     sp.o = o;
+    sp.o32 = o32;
     sp.lse = lse;
     uint8_t* w8 = static_cast<uint8_t*>(ws);
     const bool parts = wl.total > 0;
@@ -1174,6 +1192,120 @@ extern "C" int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint1
     }
     return decode::run(q, k, v, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, ns, ws, bytes,
                        stream);
+}
+
+// ---------------------------------------------------------------------------
+// Sequence-parallel decode: partial results over disjoint key ranges and their
+// merge.
+//
+// Page: "ADR-0060: AHBM GQA Fused Attention kernel (Llama3-70B)", §5.3 (decode
+// with sequence parallelism: each rank sweeps its own slice of the keys) and
+// §4 (the partials meet in a log-sum-exp reduce-to-root, normalised once at
+// the root). Here a partial is normalised over its own keys and carried as
+// (O_r fp32, lse_r); merging R of them in rank order gives
+//   lse = ln sum_r exp(lse_r),  O = sum_r exp(lse_r - lse) O_r,
+// which is the §4 merge with m = lse_r, l = 1.
+
+namespace gqa {
+namespace decode {
+
+constexpr int kMergeWarps = 8;
+
+// One warp per output row: lane r < R holds part r's lse (in chunks of 32);
+// the O parts are folded in rank order with vector loads.
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts,
+                 uint16_t* o, float* lse, int R, int rows) {
+    constexpr int kPer = D / 32;
+    using VecT = typename std::conditional<kPer == 4, float4, float2>::type;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float mx = -INFINITY;
+    for (int r = lane; r < R; r += 32) mx = fmaxf(mx, lse_parts[size_t(r) * rows + row]);
+    mx = warp_max(mx);
+    uint16_t* out = o + size_t(row) * D + lane * kPer;
+    if (mx == -INFINITY) {  // no part saw a key
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) out[j] = 0;
+        if (lane == 0 && lse) lse[row] = -INFINITY;
+        return;
+    }
+    float acc[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
+    float wsum = 0.f;
+    for (int base = 0; base < R; base += 32) {
+        const int cnt = min(32, R - base);
+        const float lr = lane < cnt ? lse_parts[size_t(base + lane) * rows + row] : -INFINITY;
+        const float w = lr == -INFINITY ? 0.f : exp2f((lr - mx) * kLog2e);
+        wsum += w;
+        for (int r = 0; r < cnt; ++r) {
+            const float wr = __shfl_sync(0xffffffffu, w, r);
+            if (wr == 0.f) continue;  // an empty part (its O may hold anything)
+            const VecT v = *reinterpret_cast<const VecT*>(
+                o_parts + (size_t(base + r) * rows + row) * D + lane * kPer);
+            const float* f = reinterpret_cast<const float*>(&v);
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) acc[j] += wr * f[j];
+        }
+    }
+    const float wtot = warp_sum(wsum);
+    const float inv = 1.f / wtot;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) out[j] = to_bf16_bits(acc[j] * inv);
+    if (lane == 0 && lse) lse[row] = mx + logf(wtot);
+}
+
+}  // namespace decode
+}  // namespace gqa
+
+extern "C" int gqa_attn_decode_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                       float* o_part, float* lse_part, const int32_t* seqlens,
+                                       int B, int H_q, int H_kv, int d, int S_max, float scale,
+                                       int num_splits, cudaStream_t stream) {
+    if (!lse_part || (reinterpret_cast<uintptr_t>(lse_part) & 3u)) return GQA_ERR_INVALID_ARG;
+    int rc = decode::check_args(q, k, v, o_part, B, H_q, H_kv, d, S_max, scale, num_splits);
+    if (rc != GQA_OK) return rc;
+    if (B == 0) return GQA_OK;
+    int ns = num_splits;
+    if (ns == 0) {
+        const int sms = num_sms();
+        if (sms <= 0) return GQA_ERR_CUDA;
+        ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
+        if (ns < 1) return GQA_ERR_INVALID_ARG;
+    }
+    const size_t bytes =
+        decode::ws_layout(B, H_q, d, ns, decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
+            .total;
+    void* ws = nullptr;
+    if (bytes > 0) {
+        ws = stream_workspace(stream, bytes);
+        if (!ws) return GQA_ERR_WORKSPACE;
+    }
+    return decode::run(q, k, v, nullptr, lse_part, seqlens, B, H_q, H_kv, d, S_max, scale, ns,
+                       ws, bytes, stream, /*ring=*/false, nullptr, nullptr, o_part);
+}
+
+extern "C" int gqa_attn_merge(const float* o_parts, const float* lse_parts, uint16_t* o,
+                              float* lse, int R, int rows, int d, cudaStream_t stream) {
+    if (!o_parts || !lse_parts || !o || R < 1 || rows < 0) return GQA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+    if (int64_t(R) * rows * d >= (int64_t(1) << 40)) return GQA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(o_parts) & 15u) || (reinterpret_cast<uintptr_t>(o) & 15u) ||
+        (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return GQA_ERR_MISALIGNED;
+    if (rows == 0) return GQA_OK;
+    const dim3 grid(unsigned((rows + decode::kMergeWarps - 1) / decode::kMergeWarps));
+    if (d == 128)
+        decode::merge_kernel<128><<<grid, decode::kMergeWarps * 32, 0, stream>>>(
+            o_parts, lse_parts, o, lse, R, rows);
+    else
+        decode::merge_kernel<64><<<grid, decode::kMergeWarps * 32, 0, stream>>>(
+            o_parts, lse_parts, o, lse, R, rows);
+    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------

@@ -141,6 +141,39 @@ int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t
                             int B, int H_q, int H_kv, int d, int S_max,
                             float scale, int num_splits, cudaStream_t stream);
 
+/* ------------------------------------------ sequence-parallel decode ------
+ * Page: ADR-0060 §5.3 (decode with sequence parallelism: every rank sweeps its
+ * own slice of the keys) and §4 (the partials meet in a log-sum-exp
+ * reduce-to-root, normalised once at the root). A sequence can be cut into R
+ * contiguous key ranges, one per device or stream: slice r of every row is
+ * [start_r, end_r) from gqa_attn_split_bounds(S_max, R, S_max, ...), and a row
+ * of length seqlen has max(0, min(seqlen, end_r) - start_r) keys in it. Each
+ * slice is decoded on its own into a partial (O_r normalised over the slice's
+ * keys, lse_r), and gqa_attn_merge folds the R partials into the result. Only
+ * (d + 1) * 4 bytes per (row, query head) move between ranks. */
+
+/* gqa_attn_decode over one slice, with the output kept in fp32 for the merge:
+ * arguments, split plan, workspace and errors as gqa_attn_decode, where k and
+ * v are the slice's own cache [B, H_kv, S_max, d] (S_max = the slice length)
+ * and seqlens the rows' key counts inside it.
+ *   o_part   : fp32 [B, H_q, d], 16-byte aligned; a row with no keys gets 0.
+ *   lse_part : fp32 [B, H_q] (required); a row with no keys gets -inf. */
+int gqa_attn_decode_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            float* o_part, float* lse_part, const int32_t* seqlens,
+                            int B, int H_q, int H_kv, int d, int S_max, float scale,
+                            int num_splits, cudaStream_t stream);
+
+/* Merges R partials in rank order with the log-sum-exp rule:
+ *   lse = ln sum_r exp(lse_r),  O = sum_r exp(lse_r - lse) O_r  (then bf16).
+ *   o_parts   : fp32 [R, rows, d] (16-byte aligned), rows = B * H_q;
+ *   lse_parts : fp32 [R, rows]; a part with lse_r = -inf (no keys) is skipped
+ *               whatever its O_r holds;
+ *   o         : bf16 [rows, d]; lse: fp32 [rows] or NULL.
+ * A row whose parts are all empty gets O = 0 and lse = -inf. d in {64, 128},
+ * R >= 1. Async on `stream`; deterministic (fixed order). */
+int gqa_attn_merge(const float* o_parts, const float* lse_parts, uint16_t* o, float* lse,
+                   int R, int rows, int d, cudaStream_t stream);
+
 /* ------------------------------------------ ring-buffer cache with sinks --
  * Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §2 item 4 (a KV
  * cache of fixed max_tokens that never grows) and §4 item 2 (once it wraps,

@@ -239,3 +239,21 @@ def test_debug_tile_counts_need_the_debug_build(L):
     # touches nothing (no device work either)
     rc, counts = api.gqa_attn_debug_tile_counts(clear=True)
     assert rc == api.GQA_ERR_UNSUPPORTED and counts == [0, 0, 0]
+
+
+def test_merge_and_partial_bad_args_return_codes_without_launch(L):
+    st = None
+    # o_parts, lse_parts, o, lse, R, rows, d
+    assert api.gqa_attn_merge(FAKE, FAKE, FAKE, FAKE, 0, 8, 64, st) == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_merge(0, FAKE, FAKE, FAKE, 2, 8, 64, st) == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_merge(FAKE, FAKE, FAKE, FAKE, 2, -1, 64, st) == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_merge(FAKE, FAKE, FAKE, FAKE, 2, 8, 96, st) == api.GQA_ERR_UNSUPPORTED
+    assert api.gqa_attn_merge(FAKE + 4, FAKE, FAKE, FAKE, 2, 8, 64, st) == api.GQA_ERR_MISALIGNED
+    assert api.gqa_attn_merge(FAKE, FAKE, FAKE, FAKE, 2, 0, 64, st) == 0  # nothing to merge
+    # q, k, v, o_part, lse_part, seqlens, B, H_q, H_kv, d, S_max, scale, num_splits
+    assert api.gqa_attn_decode_partial(FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, 0,
+                                       st) == api.GQA_ERR_INVALID_ARG      # lse is required
+    assert api.gqa_attn_decode_partial(FAKE, FAKE, FAKE, FAKE + 8, FAKE, 0, 1, 8, 1, 64, 256,
+                                       0.125, 0, st) == api.GQA_ERR_MISALIGNED
+    assert api.gqa_attn_decode_partial(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 8, 1, 64, 256, 0.125,
+                                       0, st) == 0                         # empty batch
