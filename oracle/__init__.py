@@ -11,6 +11,7 @@ from .gqa_oracle import (  # noqa: F401
     TILE_ALL_PAST,
     TILE_PARTIAL,
     attention,
+    attention_q4,
     attention_q8,
     attention_ring,
     attention_rows,
@@ -21,6 +22,7 @@ from .gqa_oracle import (  # noqa: F401
     lse_merge,
     online_softmax_sweep,
     prefill_tile_classes,
+    quantize_q4,
     quantize_q8,
     ring_slot,
     ring_visible_tokens,

@@ -447,3 +447,42 @@ def attention_q8(q, k_codes, k_scales, v_codes, v_scales, *, scale: float, seqle
     V = dequantize_q8(v_codes, v_scales)
     O, lse = attention(to_f64(q)[:, :, None, :], K, V, scale=scale, seqlens=seqlens)
     return O[:, :, 0], lse[:, :, 0]
+
+
+# ---------------------------------------------------------------------------
+# INT4 KV cache (the other half of the same recommendation).
+#
+# Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §4 item 3
+# (optional INT4 / INT8 KV quantisation for long contexts; no scheme given).
+# Reading: the INT8 scheme above with 4-bit codes: per (batch row, KV head,
+# token) one fp32 scale max|x| / 7, codes rint(x / scale) in [-7, 7] with ties
+# to even, both divisions single fp32 divisions, an all-zero token with scale
+# 0 and codes 0. Dequantised values are code * scale, exact in fp64.
+# ---------------------------------------------------------------------------
+
+
+def quantize_q4(x):
+    """x: [..., d] (any real dtype; bf16 values widen exactly to fp32).
+    Returns (codes int8 in [-7, 7] [..., d], scales float32 [...])."""
+    xf = np.asarray(to_f64(x), dtype=np.float32)
+    amax = np.max(np.abs(xf), axis=-1)
+    scale = (amax / np.float32(7.0)).astype(np.float32)
+    nz = scale > 0
+    safe = np.where(nz, scale, np.float32(1.0)).astype(np.float32)
+    codes = np.rint(xf / safe[..., None]).astype(np.float32)
+    codes = np.clip(codes, -7, 7)
+    codes = np.where(nz[..., None], codes, 0)
+    return codes.astype(np.int8), scale
+
+
+def attention_q4(q, k_codes, k_scales, v_codes, v_scales, *, scale: float, seqlens=None):
+    """Decode attention over an INT4 cache, by its definition: the plain decode
+    definition applied to the dequantised K and V (codes * scale).
+
+    q: [B, H_q, d]; k_codes, v_codes: [B, H_kv, S, d] int8 codes in [-7, 7]
+    (token-major); k_scales, v_scales: [B, H_kv, S]. Returns O [B, H_q, d],
+    lse [B, H_q]."""
+    K = np.asarray(k_codes, dtype=np.float64) * np.asarray(k_scales, dtype=np.float64)[..., None]
+    V = np.asarray(v_codes, dtype=np.float64) * np.asarray(v_scales, dtype=np.float64)[..., None]
+    O, lse = attention(to_f64(q)[:, :, None, :], K, V, scale=scale, seqlens=seqlens)
+    return O[:, :, 0], lse[:, :, 0]
