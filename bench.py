@@ -580,27 +580,31 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     graph_call = None  # decode cases: the same call in a CUDA graph over rotating caches
     extra = None
-    if args.case in ("decode8k_q8", "ragged128k_q8"):
-        # INT8 cache: bytes read are the codes plus one fp32 scale per token for
-        # K and for V; the rate is also given as the bf16 bytes it replaces
-        w = wl.RAGGED_DECODE_128K if args.case == "ragged128k_q8" else wl.LLAMA70B_DECODE_8K
+    if args.case in ("decode8k_q8", "ragged128k_q8", "decode8k_q4", "ragged128k_q4"):
+        # INT8 / INT4 cache: bytes read are the codes plus one fp32 scale per
+        # token for K and for V; the rate is also given as the bf16 bytes it
+        # replaces
+        int4 = args.case.endswith("_q4")
+        quant = api.quantize_kv_q4 if int4 else api.quantize_kv_q8
+        dec = api.decode_q4 if int4 else api.decode_q8
+        w = wl.RAGGED_DECODE_128K if args.case.startswith("ragged") else wl.LLAMA70B_DECODE_8K
         q, k, v, sl = (t.to(dev) for t in wl.decode_inputs(w))
-        caches = [api.quantize_kv_q8(k, v)]
+        caches = [quant(k, v)]
         del k, v
         tokens = sum(min(int(x), w.S_max) for x in sl.tolist())
-        q8_bytes = tokens * w.H_kv * (2 * w.d + 8)
+        q8_bytes = tokens * w.H_kv * ((w.d if int4 else 2 * w.d) + 8)
         bf16_bytes = tokens * w.H_kv * 2 * w.d * 2
         per_set = sum(t.numel() * t.element_size() for t in caches[0])
         for _ in range(max(1, -(-300_000_000 // per_set)) - 1):
             kk = torch.randn(w.B, w.H_kv, w.S_max, w.d, device=dev).to(torch.bfloat16)
             vv = torch.randn(w.B, w.H_kv, w.S_max, w.d, device=dev).to(torch.bfloat16)
-            caches.append(api.quantize_kv_q8(kk, vv))
+            caches.append(quant(kk, vv))
             del kk, vv
         torch.cuda.synchronize()
         api.check()
 
         def one(cset):
-            api.decode_q8(q, *cset, sl, num_splits=args.num_splits)
+            dec(q, *cset, sl, num_splits=args.num_splits)
 
         def call():
             one(caches[0])
@@ -620,7 +624,8 @@ def run_case(args):
 
         graph_calls = len(caches)
         work, unit = q8_bytes / 1e9, "GB/s"
-        extra = {"int8_bytes_per_call": q8_bytes, "bf16_equivalent_bytes_per_call": bf16_bytes}
+        extra = {("int4" if int4 else "int8") + "_bytes_per_call": q8_bytes,
+                 "bf16_equivalent_bytes_per_call": bf16_bytes}
     elif args.case in ("decode8k", "ragged128k", "ring8k"):
         w = wl.RAGGED_DECODE_128K if args.case == "ragged128k" else wl.LLAMA70B_DECODE_8K
         q, k, v, sl = (t.to(dev) for t in wl.decode_inputs(w))
@@ -720,7 +725,9 @@ def main():
                     help="CPU work per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="decode8k | ragged128k | prefill8k | chunked32k: one workload alone")
+                    help="decode8k | ragged128k | ring8k | decode8k_q8 | ragged128k_q8 | "
+                         "decode8k_q4 | ragged128k_q4 | prefill8k | chunked32k: one workload "
+                         "alone")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-worker-steps", type=int, default=1, help=argparse.SUPPRESS)

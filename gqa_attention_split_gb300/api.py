@@ -49,6 +49,9 @@ _SIGNATURES = {
     "gqa_attn_prefill_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_pick_num_splits": (_I, [_I, _I, _I, _I]),
     "gqa_attn_pick_num_splits_q8": (_I, [_I, _I, _I, _I]),
+    "gqa_attn_pick_num_splits_q4": (_I, [_I, _I, _I, _I]),
+    "gqa_attn_quantize_kv_q4": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "gqa_attn_decode_q4": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "gqa_attn_decode_cluster_size": (_I, [_I, _I, _I, _I]),
     "gqa_attn_split_bounds": (_I, [_I, _I, _I, _P, _P]),
     "gqa_attn_tile_class": (_I, [_I, _I, _I, _I]),
@@ -148,6 +151,21 @@ def gqa_attn_pick_num_splits(B, H_kv, S_max, num_sms):
 
 def gqa_attn_pick_num_splits_q8(B, H_kv, S_max, num_sms):
     return lib().gqa_attn_pick_num_splits_q8(B, H_kv, S_max, num_sms)
+
+
+def gqa_attn_pick_num_splits_q4(B, H_kv, S_max, num_sms):
+    return lib().gqa_attn_pick_num_splits_q4(B, H_kv, S_max, num_sms)
+
+
+def gqa_attn_quantize_kv_q4(k, v, k_codes, v_codes, k_scales, v_scales, B, H_kv, S, d, stream):
+    return lib().gqa_attn_quantize_kv_q4(k, v, k_codes, v_codes, k_scales, v_scales, B, H_kv, S,
+                                         d, stream)
+
+
+def gqa_attn_decode_q4(q, k_codes, v_codes, k_scales, v_scales, o, lse, seqlens, B, H_q, H_kv, d,
+                       S_max, scale, num_splits, stream):
+    return lib().gqa_attn_decode_q4(q, k_codes, v_codes, k_scales, v_scales, o, lse, seqlens, B,
+                                    H_q, H_kv, d, S_max, scale, num_splits, stream)
 
 
 def gqa_attn_decode_cluster_size(B, H_kv, num_splits, num_sms):
@@ -401,6 +419,60 @@ def decode_q8(q, k_codes, v_codes, k_scales, v_scales, seqlens=None, *, num_spli
                             S_max, sc, num_splits, _stream_ptr(stream))
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_attn_decode_q8")
+    return out, lse
+
+
+def quantize_kv_q4(k, v, *, stream=None):
+    """INT4 cache from a bf16 cache k, v [B,H_kv,S,d] (CUDA): returns
+    (k_codes [B,H_kv,S,d/2], v_codes [B,H_kv,d,S/2] as uint8, two nibbles
+    code + 8 per byte, k_scales, v_scales [B,H_kv,S] fp32)."""
+    import torch
+
+    _check_cuda_bf16("k", k, 4)
+    _check_cuda_bf16("v", v, 4)
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    B, H_kv, S, d = k.shape
+    kc = torch.empty((B, H_kv, S, d // 2), dtype=torch.uint8, device=k.device)
+    vc = torch.empty((B, H_kv, d, S // 2), dtype=torch.uint8, device=k.device)
+    ks = torch.empty((B, H_kv, S), dtype=torch.float32, device=k.device)
+    vs = torch.empty_like(ks)
+    rc = gqa_attn_quantize_kv_q4(_ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), B, H_kv,
+                                 S, d, _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_quantize_kv_q4")
+    return kc, vc, ks, vs
+
+
+def decode_q4(q, k_codes, v_codes, k_scales, v_scales, seqlens=None, *, num_splits: int = 0,
+              scale: float | None = None, out=None, lse=None, stream=None):
+    """Split-KV decode over an INT4 cache (layouts as ``quantize_kv_q4``).
+    Returns (o [B,H_q,d] bf16, lse [B,H_q] fp32)."""
+    import torch
+
+    _check_cuda_bf16("q", q, 3)
+    B, H_q, d = q.shape
+    H_kv, S_max = k_codes.shape[1], k_codes.shape[2]
+    if (k_codes.dtype != torch.uint8 or v_codes.dtype != torch.uint8
+            or k_codes.shape != (B, H_kv, S_max, d // 2)
+            or v_codes.shape != (B, H_kv, d, S_max // 2)):
+        raise ValueError("k_codes [B,H_kv,S,d/2] and v_codes [B,H_kv,d,S/2] must be uint8")
+    for nm, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        if t.dtype != torch.float32 or t.shape != (B, H_kv, S_max) or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous fp32 [B, H_kv, S] tensor")
+    if seqlens is not None and (seqlens.dtype != torch.int32 or not seqlens.is_cuda
+                                or seqlens.numel() != B):
+        raise TypeError("seqlens must be an int32 CUDA tensor of B elements")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = gqa_attn_decode_q4(_ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+                            _ptr(v_scales), _ptr(out), _ptr(lse), _ptr(seqlens), B, H_q, H_kv, d,
+                            S_max, sc, num_splits, _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_decode_q4")
     return out, lse
 
 

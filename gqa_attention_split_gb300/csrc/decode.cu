@@ -81,19 +81,24 @@ struct SplitParams {
 
 // Q8: the cache holds int8 codes, K token-major [S][D] and V dim-major
 // [D][S], with one fp32 scale per token for each (see gqa_attn_decode_q8).
-template <int D, int TILE_T, int STAGES, int WARPS, bool Q8 = false>
+// Q4: int4 codes, two per byte, K token-major [S][D/2] and V dim-major
+// [D][S/2], scales as Q8 (see gqa_attn_decode_q4).
+template <int D, int TILE_T, int STAGES, int WARPS, bool Q8 = false, bool Q4 = false>
 struct SplitCfg {
+    static constexpr bool kQuant = Q8 || Q4;
     static constexpr int kThreads = WARPS * 32;
     static constexpr int kBoxes = D / 64;               // bf16: 128-byte column boxes per row
     static constexpr int kBoxBytes = TILE_T * 128;      // bf16: one box, TILE_T rows x 128 B
-    static constexpr int kKBytes = Q8 ? TILE_T * D : kBoxes * kBoxBytes;  // K part of a stage
-    static constexpr int kVBytes = Q8 ? D * TILE_T : kKBytes;             // V (or V^T) part
+    static constexpr int kKBytes = Q4   ? TILE_T * D / 2
+                                   : Q8 ? TILE_T * D
+                                        : kBoxes * kBoxBytes;  // K part of a stage
+    static constexpr int kVBytes = kKBytes;  // V (or V^T) part: the same size
     static constexpr int kStageBytes = kKBytes + kVBytes;
     static constexpr int kRingBytes = WARPS * STAGES * kStageBytes;
-    // Q8: per-token scales of K and V for every stage, [WARPS][STAGES][2][TILE_T]
+    // int8 / int4: per-token scales of K and V for every stage, [WARPS][STAGES][2][TILE_T]
     static constexpr int kScaleOffset = kRingBytes;
-    static constexpr int kScaleBytes = Q8 ? WARPS * STAGES * 2 * TILE_T * 4 : 0;
-    static constexpr int kTxBytes = kStageBytes + (Q8 ? 2 * TILE_T * 4 : 0);  // per stage
+    static constexpr int kScaleBytes = kQuant ? WARPS * STAGES * 2 * TILE_T * 4 : 0;
+    static constexpr int kTxBytes = kStageBytes + (kQuant ? 2 * TILE_T * 4 : 0);  // per stage
     // Per-head record a CTA sends to the head's owner in the cluster:
     // {m, l, 0, 0, O[0..D)} as floats (16 + 4*D bytes, a multiple of 16).
     static constexpr int kRec = 4 + D;
@@ -115,6 +120,7 @@ struct SplitCfg {
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(!Q8 || (D == 128 && (TILE_T == 32 || TILE_T == 64 || TILE_T == 128)),
                   "int8 tiles: 32, 64 or 128 tokens of a 128-dim head");
+    static_assert(!Q4 || (D == 128 && TILE_T == 64 && !Q8), "int4 tiles: 64 tokens, d = 128");
     static_assert(kStageBytes % 1024 == 0, "stages stay aligned for the TMA swizzle");
 };
 
@@ -171,13 +177,14 @@ __device__ __forceinline__ void emit(const SplitParams& p, size_t row, int gi, i
     }
 }
 
-template <int D, int TILE_T, int STAGES, int WARPS, int CS, bool Q8>
+template <int D, int TILE_T, int STAGES, int WARPS, int CS, bool Q8, bool Q4 = false>
 __global__ void __launch_bounds__(WARPS * 32, 1)
     split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v,
                  const __grid_constant__ CUtensorMap tmap_ks,
                  const __grid_constant__ CUtensorMap tmap_vs, const SplitParams p) {
-    using C = SplitCfg<D, TILE_T, STAGES, WARPS, Q8>;
+    using C = SplitCfg<D, TILE_T, STAGES, WARPS, Q8, Q4>;
+    constexpr bool kQ = C::kQuant;  // int8 or int4 codes with per-token scales
     const int s = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
     const int gi = s / CS;         // cluster (group) index within the row
     const int rank = s % CS;       // == %cluster_ctarank for a (CS, 1, 1) cluster
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
-        if constexpr (Q8) {
+        if constexpr (kQ) {
             tma_prefetch_desc(&tmap_ks);
             tma_prefetch_desc(&tmap_vs);
         }
@@ -230,22 +237,22 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         int hint = p.seqlens ? *reinterpret_cast<const volatile int32_t*>(p.seqlens + b) : p.S_max;
         hint = hint < 0 ? 0 : (hint > p.S_max ? p.S_max : hint);
         const SplitRange rh = split_range(p.L, s, hint);
-        // bf16 tiles start at the split's first key; int8 tiles sit on
-        // TILE_T-aligned keys (see below)
-        const int hbase = Q8 ? rh.start - rh.start % TILE_T : rh.start;
+        // bf16 tiles start at the split's first key; int8 / int4 tiles sit
+        // on TILE_T-aligned keys (see below)
+        const int hbase = kQ ? rh.start - rh.start % TILE_T : rh.start;
         const int nt = rh.end > rh.start ? (rh.end - hbase + TILE_T - 1) / TILE_T : 0;
         const int mine = warp < nt ? (nt - warp + WARPS - 1) / WARPS : 0;
-        constexpr int kPf = Q8 ? 4 : 2 * C::kBoxes;  // the copies of one tile
+        constexpr int kPf = kQ ? 4 : 2 * C::kBoxes;  // the copies of one tile
         static_assert(GQA_DEC_WARM_TILES * kPf <= 32, "one lane per prefetch");
         if (lane < min(GQA_DEC_WARM_TILES, mine) * kPf) {
             const int i = lane / kPf, j = lane % kPf;
             const int tok0 = hbase + (warp + i * WARPS) * TILE_T;
             const int z = b * p.H_kv + kv;
-            if constexpr (Q8) {
+            if constexpr (kQ) {
                 if (j == 0)
                     tma_prefetch_l2_3d(&tmap_k, 0, tok0, z);
-                else if (j == 1)
-                    tma_prefetch_l2_3d(&tmap_v, tok0, 0, z);
+                else if (j == 1)  // int4: two tokens per byte of a V row
+                    tma_prefetch_l2_3d(&tmap_v, Q4 ? tok0 / 2 : tok0, 0, z);
                 else
                     tma_prefetch_l2_2d(j == 2 ? &tmap_ks : &tmap_vs, tok0, z);
             } else {
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // (a TMA box of the dim-major V codes must start on a 16-byte boundary);
     // keys of a tile outside [r.start, r.end) are masked, and padding codes are
     // finite, so no P = 0 row can turn into NaN.
-    const int base = Q8 ? r.start - r.start % TILE_T : r.start;
+    const int base = kQ ? r.start - r.start % TILE_T : r.start;
     const int n_tiles = len > 0 ? (r.end - base + TILE_T - 1) / TILE_T : 0;
     const int my_n = warp < n_tiles ? (n_tiles - warp + WARPS - 1) / WARPS : 0;
     const int zc = b * p.H_kv + kv;  // outer TMA coordinate: (batch, KV head)
@@ -292,20 +299,20 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     };
     float* scales = reinterpret_cast<float*>(smem + C::kScaleOffset);  // int8 only
     // A bf16 stage is 2 * kBoxes copies (K and V, 64 columns each); an int8
-    // stage is K codes, V codes, K scales, V scales. Lane 0 arms the stage's
-    // barrier, then each copy goes out from its own lane.
-    constexpr int kCopies = Q8 ? 4 : 2 * C::kBoxes;
+    // or int4 stage is K codes, V codes, K scales, V scales. Lane 0 arms the
+    // stage's barrier, then each copy goes out from its own lane.
+    constexpr int kCopies = kQ ? 4 : 2 * C::kBoxes;
     static_assert(STAGES * kCopies <= 32, "one lane per copy of the first stages");
     auto copy = [&](int i, int j) {
         const int slot = i % STAGES;
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t stage = smem_u32(ring + slot * C::kStageBytes);
-        if constexpr (Q8) {
+        if constexpr (kQ) {
             const int t0 = base + (warp + i * WARPS) * TILE_T;
             if (j == 0)
                 tma_load_3d(stage, &tmap_k, 0, t0, zc, bar, policy);
-            else if (j == 1)
-                tma_load_3d(stage + C::kKBytes, &tmap_v, t0, 0, zc, bar, policy);
+            else if (j == 1)  // int4: the V row's x coordinate is in bytes, t0 / 2
+                tma_load_3d(stage + C::kKBytes, &tmap_v, Q4 ? t0 / 2 : t0, 0, zc, bar, policy);
             else
                 tma_load_2d(smem_u32(scales + ((warp * STAGES + slot) * 2 + (j - 2)) * TILE_T),
                             j == 2 ? &tmap_ks : &tmap_vs, t0, zc, bar, policy);
@@ -334,19 +341,25 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // q^T as the B operand (k = head dim, n = query head g of this group).
     // int8: f16 pairs, with the head dims in the order the K words are read
     // (k step kc of lane c takes dims 32c + 4kc .. +3; see the S MMA below).
+    // int4: k step kc of lane c takes dims 32c + 8(kc/2) + 2(kc%2) + {0, 4}
+    // (first pair) and + {1, 5} (second pair, divided by 16: those K codes
+    // come out of nib_pair_hi as 16 x code).
     // Before the conversion each head is scaled by a power of two 2^e that puts
     // its largest |q| in [2^14, 2^15): the f16 operands then hold every bf16 bit
     // of q whatever its magnitude (unscaled, |q| > 65504 would overflow f16 and
     // tiny q would fall into its subnormals). 2^-e comes off with the K scale.
     uint32_t qf[C::kKC][2];
-    float qsum = 0.f;  // int8: this lane's share of sum_d q[g][d] (scaled f16 values)
-    [[maybe_unused]] float hs0 = p.scale_log2, hs1 = p.scale_log2;  // int8: heads 2c, 2c+1
+    // int8 / int4: this lane's share of sum_d offset_d * q'[g][d] over the f16
+    // values q' the MMA sees, where offset_d is what the K code of dim d
+    // carries on top of the code (see qoff below)
+    float qsum = 0.f;
+    [[maybe_unused]] float hs0 = p.scale_log2, hs1 = p.scale_log2;  // quantised: heads 2c, 2c+1
     {
         const bool has = g < p.G;
         const uint16_t* qh = p.q + (size_t(b) * p.H_q + kv * p.G + (has ? g : 0)) * D;
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qh);
-        if constexpr (Q8) {
-            uint2 w[C::kKC];
+        if constexpr (kQ) {
+            uint2 w[C::kKC];  // dims 32c + 4j .. +3 in w[j]
             float amax = 0.f;
 #pragma unroll
             for (int kc = 0; kc < C::kKC; ++kc) {
@@ -364,15 +377,37 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             const int e = amax > 0.f ? min(max(141 - ebits, -126), 126) : 0;
             const float up = __uint_as_float(uint32_t(e + 127) << 23);    // 2^e
             const float down = __uint_as_float(uint32_t(127 - e) << 23);  // 2^-e
+            if constexpr (Q8) {
 #pragma unroll
-            for (int kc = 0; kc < C::kKC; ++kc) {
-                qf[kc][0] = pack_f16x2(__uint_as_float(w[kc].x << 16) * up,
-                                       __uint_as_float(w[kc].x & 0xFFFF0000u) * up);
-                qf[kc][1] = pack_f16x2(__uint_as_float(w[kc].y << 16) * up,
-                                       __uint_as_float(w[kc].y & 0xFFFF0000u) * up);
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][0]));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][1]));
-                qsum += (f0.x + f0.y) + (f1.x + f1.y);
+                for (int kc = 0; kc < C::kKC; ++kc) {
+                    qf[kc][0] = pack_f16x2(__uint_as_float(w[kc].x << 16) * up,
+                                           __uint_as_float(w[kc].x & 0xFFFF0000u) * up);
+                    qf[kc][1] = pack_f16x2(__uint_as_float(w[kc].y << 16) * up,
+                                           __uint_as_float(w[kc].y & 0xFFFF0000u) * up);
+                    const float2 f0 =
+                        __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][0]));
+                    const float2 f1 =
+                        __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][1]));
+                    qsum += (f0.x + f0.y) + (f1.x + f1.y);
+                }
+            } else {
+                const float up16 = up * 0.0625f;
+                // word m of the lane's dims: dims 32c + 2m (low half), 32c + 2m + 1
+                auto qw = [&](int m) { return (m & 1) ? w[m >> 1].y : w[m >> 1].x; };
+#pragma unroll
+                for (int kc = 0; kc < C::kKC; ++kc) {
+                    const uint32_t wa = qw(4 * (kc >> 1) + (kc & 1));  // dims +0, +1
+                    const uint32_t wb = qw(4 * (kc >> 1) + (kc & 1) + 2);  // dims +4, +5
+                    qf[kc][0] = pack_f16x2(__uint_as_float(wa << 16) * up,
+                                           __uint_as_float(wb << 16) * up);
+                    qf[kc][1] = pack_f16x2(__uint_as_float(wa & 0xFFFF0000u) * up16,
+                                           __uint_as_float(wb & 0xFFFF0000u) * up16);
+                    const float2 f0 =
+                        __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][0]));
+                    const float2 f1 =
+                        __half22float2(*reinterpret_cast<const __half2*>(&qf[kc][1]));
+                    qsum += kQ4OffsetLo * (f0.x + f0.y) + kQ4OffsetHi * (f1.x + f1.y);
+                }
             }
             hs0 = p.scale_log2 * __shfl_sync(0xffffffffu, down, 8 * c);      // head 2c
             hs1 = p.scale_log2 * __shfl_sync(0xffffffffu, down, 8 * c + 4);  // head 2c + 1
@@ -385,16 +420,20 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
     }
 
-    // int8: the f16 codes are code + 1152, so the S MMA adds 1152 * sum_d q[h][d]
+    // int8: the f16 codes are code + 1152, so the S MMA adds 1152 * sum_d q'[h][d]
     // to head h's scores (qoff, taken off before scaling) and the P.V MMA adds
     // 1152 * sum_k P'[h][k] to every dim of head h (poff, this lane's share of
     // the running sum of the f16 P' it fed the MMA; taken off at the end).
+    // int4: the same with the offsets of its conversions, 1032 and 1152
+    // (16 x 72) per K position and 1152 for every V value, which qsum and poff
+    // already carry.
     float qoff0 = 0.f, qoff1 = 0.f, poff0 = 0.f, poff1 = 0.f;
-    if constexpr (Q8) {
+    if constexpr (kQ) {
+        constexpr float kQScale = Q8 ? kQ8Offset : 1.f;
         qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
         qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // lanes 4g .. 4g+3: head g
-        qoff0 = kQ8Offset * __shfl_sync(0xffffffffu, qsum, 8 * c);
-        qoff1 = kQ8Offset * __shfl_sync(0xffffffffu, qsum, 8 * c + 4);
+        qoff0 = kQScale * __shfl_sync(0xffffffffu, qsum, 8 * c);
+        qoff1 = kQScale * __shfl_sync(0xffffffffu, qsum, 8 * c + 4);
     }
     float m0 = -INFINITY, m1 = -INFINITY;  // heads 2c, 2c+1 (base-2 domain)
     float l0 = 0.f, l1 = 0.f;               // this lane's share of the row sums
@@ -412,7 +451,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             if (alive) waited = i + 1;                // copies observed complete so far
         }
         if (i == 0 && threadIdx.x == 0) GQA_TRACE_STAMP(blin, 2);
-        if constexpr (!Q8) {
+        if constexpr (!kQ) {
             const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
             const uint32_t vbase = kbase + C::kKBytes;
             const int tok0 = r.start + (warp + i * WARPS) * TILE_T;
@@ -493,7 +532,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 }
             }
 
-        } else {
+        } else if constexpr (Q8) {
             // int8 codes: K rows are tokens [TILE_T][128 B] (128-byte swizzle),
             // V rows are head dims [D][TILE_T B] (64-byte swizzle). m-tile mt of
             // the MMAs takes logical key m = 2c' + h (+8) to tile key
@@ -636,6 +675,152 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                     mma_f16_16816(acc[md], a, b_lo[kt], b_hi[kt]);
                 }
             }
+        } else {
+            // int4 codes, two per byte (the lower token or dim in the low
+            // nibble): K rows are tokens [TILE_T][64 B], V rows are head dims
+            // [D][32 B], both unswizzled. m-tile mt of the MMAs takes logical key
+            // m = 2c' + h (+8) from tile key 16c' + mt + 4h (+8): then a lane's
+            // P.V operand keys (logical 2c, 2c+1, 2c+8, 2c+9) in m-tile mt are
+            // nibbles mt and mt + 4 of the two words holding keys 16c .. 16c+15
+            // of a V row, one 8-byte load per dim row for all four m-tiles.
+            // Every V nibble is shifted to bits 4-7 and read by nib_pair_hi as
+            // 1152 + 16 x code, so P is divided by 16 throughout: the offset the
+            // P.V sums carry is then 72 per code step, near the int8 path's
+            // ratio, where nib_pair_lo's 1032 per step would leave too little
+            // of the result once the fp32 sums over thousands of keys cancel it.
+            // The K side keeps the mixed form: its offset is one constant per
+            // head and key row, and what its rounding leaves is nearly the same
+            // for every key of a row, which the softmax takes out.
+            static_assert(TILE_T == 64, "the key order below covers 64-token tiles");
+            const uint32_t kbase = smem_u32(ring + slot * C::kStageBytes);
+            const uint32_t vbase = kbase + C::kKBytes;
+            const float* ksc = scales + (warp * STAGES + slot) * 2 * TILE_T;
+            const float* vsc = ksc + TILE_T;
+            const int tok0 = base + (warp + i * WARPS) * TILE_T;
+            const int lo = max(tok0, r.start), hi = min(tok0 + TILE_T, r.end);
+            const int kr0 = 16 * (g >> 1) + 4 * (g & 1);  // tile key of logical row g in
+                                                          // m-tile 0; row g + 8: + 8;
+                                                          // m-tile mt: + mt
+
+            // ---- S^T = K_j q^T: lane c reads dims [32c, 32c + 32) of its two
+            // key rows (one 16-byte chunk each); k step kc takes word kc / 2,
+            // shifted by 8 for odd kc.
+            float sc[C::kMT][4];
+            bool ok[C::kMT][2];
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+                const uint4 r0 = ld_shared_v4(kbase + (kr0 + mt) * 64 + c * 16);
+                const uint4 r1 = ld_shared_v4(kbase + (kr0 + mt + 8) * 64 + c * 16);
+                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+                const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int kc = 0; kc < C::kKC; ++kc) {
+                    const int sh = (kc & 1) * 8;
+                    const uint32_t x0 = w0[kc >> 1] >> sh, x1 = w1[kc >> 1] >> sh;
+                    const uint32_t a[4] = {nib_pair_lo(x0), nib_pair_lo(x1), nib_pair_hi(x0),
+                                           nib_pair_hi(x1)};
+                    mma_f16_16816(sc[mt], a, qf[kc][0], qf[kc][1]);
+                }
+            }
+
+            // ---- scale by the token's K scale, mask (select), running max
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int key = kr0 + mt + 8 * rr;
+                    const int pos = tok0 + key;
+                    ok[mt][rr] = pos >= lo && pos < hi;
+                    const float kq = ksc[key];  // the token's K scale
+                    sc[mt][2 * rr] =
+                        ok[mt][rr] ? (sc[mt][2 * rr] - qoff0) * (kq * hs0) : -INFINITY;
+                    sc[mt][2 * rr + 1] =
+                        ok[mt][rr] ? (sc[mt][2 * rr + 1] - qoff1) * (kq * hs1) : -INFINITY;
+                }
+                mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
+                mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: >= 1 key valid
+            const float corr0 = fast_exp2(m0 - mn0), corr1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                sc[mt][0] = fast_exp2(sc[mt][0] - mn0);
+                sc[mt][1] = fast_exp2(sc[mt][1] - mn1);
+                sc[mt][2] = fast_exp2(sc[mt][2] - mn0);
+                sc[mt][3] = fast_exp2(sc[mt][3] - mn1);
+                ps0 += sc[mt][0] + sc[mt][2];
+                ps1 += sc[mt][1] + sc[mt][3];
+                // P times the token's V scale and 1/16; a masked key gives
+                // exactly 0 whatever scale its slot holds
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const float f = vsc[kr0 + mt + 8 * rr] * 0.0625f;
+                    sc[mt][2 * rr] = ok[mt][rr] ? sc[mt][2 * rr] * f : 0.f;
+                    sc[mt][2 * rr + 1] = ok[mt][rr] ? sc[mt][2 * rr + 1] * f : 0.f;
+                }
+            }
+            l0 = l0 * corr0 + ps0;
+            l1 = l1 * corr1 + ps1;
+#pragma unroll
+            for (int md = 0; md < C::kKC; ++md) {
+                acc[md][0] *= corr0;
+                acc[md][1] *= corr1;
+                acc[md][2] *= corr0;
+                acc[md][3] *= corr1;
+            }
+            // P' as the MMA will see it (f16), and its per-head sums times the
+            // 1152 offset of every V value, removed at the end
+            uint32_t pp[C::kMT][2];
+            float pv0 = 0.f, pv1 = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                pp[mt][0] = pack_f16x2(sc[mt][0], sc[mt][1]);
+                pp[mt][1] = pack_f16x2(sc[mt][2], sc[mt][3]);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pp[mt][0]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pp[mt][1]));
+                pv0 += f0.x + f1.x;
+                pv1 += f0.y + f1.y;
+            }
+            pv0 *= kQ4OffsetHi;
+            pv1 *= kQ4OffsetHi;
+            poff0 = poff0 * corr0 + pv0;
+            poff1 = poff1 * corr1 + pv1;
+
+            // ---- O^T += V_j^T P^T: lane (g, c) reads keys 16c .. 16c+15 of
+            // dims md*16 + g and + 8 (8 bytes each); m-tile kt takes nibbles
+            // kt, kt + 4 of each word (low word: keys 16c .. +7, high word:
+            // keys 16c + 8 .. +15), moved to bits 4-7 and 20-23 first.
+            uint32_t b_lo[C::kMT], b_hi[C::kMT];
+#pragma unroll
+            for (int kt = 0; kt < C::kMT; ++kt) {
+                b_lo[kt] = movmatrix_trans(pp[kt][0]);
+                b_hi[kt] = movmatrix_trans(pp[kt][1]);
+            }
+#pragma unroll
+            for (int md = 0; md < C::kKC; ++md) {
+                const int d0 = md * 16 + g, d1 = d0 + 8;
+                const uint2 v0 = ld_shared_v2(vbase + d0 * (TILE_T / 2) + c * 8);
+                const uint2 v1 = ld_shared_v2(vbase + d1 * (TILE_T / 2) + c * 8);
+#pragma unroll
+                for (int kt = 0; kt < C::kMT; ++kt) {
+                    auto at4 = [&](uint32_t u) {  // nibbles kt, kt + 4 -> bits 4-7, 20-23
+                        return kt == 0 ? u << 4 : u >> (4 * (kt - 1));
+                    };
+                    const uint32_t a[4] = {nib_pair_hi(at4(v0.x)), nib_pair_hi(at4(v1.x)),
+                                           nib_pair_hi(at4(v0.y)), nib_pair_hi(at4(v1.y))};
+                    mma_f16_16816(acc[md], a, b_lo[kt], b_hi[kt]);
+                }
+            }
         }
 
         __syncwarp();
@@ -654,7 +839,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    if constexpr (Q8) {
+    if constexpr (kQ) {
+        constexpr float kPScale = Q8 ? kQ8Offset : 1.f;  // int4's sums carry their offsets
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             poff0 += __shfl_xor_sync(0xffffffffu, poff0, off);
@@ -662,10 +848,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
         }
 #pragma unroll
         for (int md = 0; md < C::kKC; ++md) {
-            acc[md][0] -= kQ8Offset * poff0;
-            acc[md][1] -= kQ8Offset * poff1;
-            acc[md][2] -= kQ8Offset * poff0;
-            acc[md][3] -= kQ8Offset * poff1;
+            acc[md][0] -= kPScale * poff0;
+            acc[md][1] -= kPScale * poff1;
+            acc[md][2] -= kPScale * poff0;
+            acc[md][3] -= kPScale * poff1;
         }
     }
     if (threadIdx.x == 0) GQA_TRACE_STAMP(blin, 3);
@@ -927,6 +1113,16 @@ constexpr int kTileT = GQA_DEC_TILE_T, kStages = GQA_DEC_STAGES, kWarps = GQA_DE
 // stages per CTA, a longer grid 3 warps x 2 stages (GB300, 8K decode: 9.4 vs
 // 9.8 us; ragged 128K batch: 106 vs 97 us).
 constexpr int kTileTQ8 = 64;
+// int4 caches: 64 tokens per stage (8 KB of codes + 512 B of scales)
+constexpr int kTileTQ4 = 64;
+#ifndef GQA_DEC_Q4_WARPS
+#define GQA_DEC_Q4_WARPS 4
+#endif
+#ifndef GQA_DEC_Q4_STAGES
+#define GQA_DEC_Q4_STAGES 2
+#endif
+constexpr int kQ4WarpsOneWave = GQA_DEC_Q4_WARPS, kQ4StagesOneWave = GQA_DEC_Q4_STAGES;
+constexpr int kQ4Warps = 3, kQ4Stages = 3;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -954,12 +1150,16 @@ WsLayout ws_layout(int B, int H_q, int d, int ns, int cs) {
     return w;
 }
 
-// maps: K, V (bf16) or K codes, V codes, K scales, V scales (int8).
-template <int D, int CS, bool Q8, int kW = kWarps, int kS = kStages>
+// Cache formats of a launch: bf16 K/V, int8 codes, int4 codes.
+enum Kind { kBf16 = 0, kInt8 = 1, kInt4 = 2 };
+
+// maps: K, V (bf16) or K codes, V codes, K scales, V scales (int8, int4).
+template <int D, int CS, int KIND, int kW = kWarps, int kS = kStages>
 int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream_t stream) {
-    constexpr int kT = Q8 ? kTileTQ8 : kTileT;
-    using C = SplitCfg<D, kT, kS, kW, Q8>;
-    auto kern = split_kernel<D, kT, kS, kW, CS, Q8>;
+    constexpr bool kQ8 = KIND == kInt8, kQ4 = KIND == kInt4;
+    constexpr int kT = kQ8 ? kTileTQ8 : kQ4 ? kTileTQ4 : kTileT;
+    using C = SplitCfg<D, kT, kS, kW, kQ8, kQ4>;
+    auto kern = split_kernel<D, kT, kS, kW, CS, kQ8, kQ4>;
     // once per device (a race only sets them twice, which is harmless)
     static std::atomic<uint64_t> attr_done{0};
     const int dev = current_device();
@@ -997,26 +1197,30 @@ int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream
     return GQA_OK;
 }
 
-template <int D, bool Q8, int kW, int kS>
+template <int D, int KIND, int kW, int kS>
 int launch_cs(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     switch (cs) {
-        case 16: return launch_split<D, 16, Q8, kW, kS>(sp, maps, stream);
-        case 8: return launch_split<D, 8, Q8, kW, kS>(sp, maps, stream);
-        case 4: return launch_split<D, 4, Q8, kW, kS>(sp, maps, stream);
-        case 2: return launch_split<D, 2, Q8, kW, kS>(sp, maps, stream);
-        default: return launch_split<D, 1, Q8, kW, kS>(sp, maps, stream);
+        case 16: return launch_split<D, 16, KIND, kW, kS>(sp, maps, stream);
+        case 8: return launch_split<D, 8, KIND, kW, kS>(sp, maps, stream);
+        case 4: return launch_split<D, 4, KIND, kW, kS>(sp, maps, stream);
+        case 2: return launch_split<D, 2, KIND, kW, kS>(sp, maps, stream);
+        default: return launch_split<D, 1, KIND, kW, kS>(sp, maps, stream);
     }
 }
 
-template <int D, bool Q8>
+template <int D, int KIND>
 int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     int rc;
-    if constexpr (Q8)
-        rc = sp.warm_l2 ? launch_cs<D, true, 4, 1>(sp, cs, maps, stream)
-                        : launch_cs<D, true, 3, 2>(sp, cs, maps, stream);
+    if constexpr (KIND == kInt8)
+        rc = sp.warm_l2 ? launch_cs<D, kInt8, 4, 1>(sp, cs, maps, stream)
+                        : launch_cs<D, kInt8, 3, 2>(sp, cs, maps, stream);
+    else if constexpr (KIND == kInt4)
+        rc = sp.warm_l2 ? launch_cs<D, kInt4, kQ4WarpsOneWave, kQ4StagesOneWave>(sp, cs, maps,
+                                                                                 stream)
+                        : launch_cs<D, kInt4, kQ4Warps, kQ4Stages>(sp, cs, maps, stream);
     else
-        rc = sp.warm_l2 ? launch_cs<D, false, kWarps, kStages>(sp, cs, maps, stream)
-                        : launch_cs<D, false, 4, 1>(sp, cs, maps, stream);
+        rc = sp.warm_l2 ? launch_cs<D, kBf16, kWarps, kStages>(sp, cs, maps, stream)
+                        : launch_cs<D, kBf16, 4, 1>(sp, cs, maps, stream);
     if (rc != GQA_OK || sp.n_groups == 1) return rc;
 
     static std::atomic<uint64_t> attr_done{0};
@@ -1064,8 +1268,11 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
         const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max, float scale,
         int ns, void* ws, size_t ws_bytes, cudaStream_t stream, bool ring = false,
         const float* k_scales = nullptr, const float* v_scales = nullptr,
-        float* o32 = nullptr) {
-    const bool q8 = k_scales != nullptr;  // k, v are then int8 K codes and dim-major V codes
+        float* o32 = nullptr, bool int4 = false) {
+    // with scales, k and v are K codes and dim-major V codes: int8, or int4
+    // (two per byte) when int4 is set
+    const bool q8 = k_scales != nullptr && !int4;
+    const bool q4 = k_scales != nullptr && int4;
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
     const int cs = cluster_size_for(ns, int64_t(ns) * H_kv * B);
@@ -1089,6 +1296,22 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
                         kTileTQ8 == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
                         : kTileTQ8 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                          : CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+            encode_tmap(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, k_scales, sd, sb,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess ||
+            encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, v_scales, sd, sb,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    } else if (q4) {
+        const uint64_t kd[3] = {uint64_t(d) / 2, uint64_t(S_max), outer};  // K codes [.., S, d/2]
+        const uint32_t kb[3] = {uint32_t(d) / 2, kTileTQ4, 1};
+        const uint64_t vd[3] = {uint64_t(S_max) / 2, uint64_t(d), outer};  // V codes [.., d, S/2]
+        const uint32_t vb[3] = {kTileTQ4 / 2, uint32_t(d), 1};
+        const uint64_t sd[2] = {uint64_t(S_max), outer};                    // scales [.., S]
+        const uint32_t sb[2] = {kTileTQ4, 1};
+        if (encode_tmap(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, k, kd, kb,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess ||
+            encode_tmap(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, v, vd, vb,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess ||
             encode_tmap(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, k_scales, sd, sb,
                         CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess ||
             encode_tmap(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, v_scales, sd, sb,
@@ -1133,9 +1356,10 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.trace_row0 = trace_row;
     trace_row += ns * H_kv * B;
 #endif
-    if (q8) return launch<128, true>(sp, cs, maps, stream);
-    return d == 128 ? launch<128, false>(sp, cs, maps, stream)
-                    : launch<64, false>(sp, cs, maps, stream);
+    if (q8) return launch<128, kInt8>(sp, cs, maps, stream);
+    if (q4) return launch<128, kInt4>(sp, cs, maps, stream);
+    return d == 128 ? launch<128, kBf16>(sp, cs, maps, stream)
+                    : launch<64, kBf16>(sp, cs, maps, stream);
 }
 
 }  // namespace decode
@@ -1517,6 +1741,130 @@ extern "C" int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes,
     return decode::run(q, reinterpret_cast<const uint16_t*>(k_codes),
                        reinterpret_cast<const uint16_t*>(v_codes), o, lse, seqlens, B, H_q, H_kv,
                        d, S_max, scale, ns, ws, bytes, stream, /*ring=*/false, k_scales, v_scales);
+}
+
+// ---------------------------------------------------------------------------
+// INT4 KV cache: the INT8 scheme with 4-bit codes (page 3, §4 item 3). Each
+// (batch row, KV head, token) of K and of V gets one fp32 scale max|x| / 7 and
+// codes rint(x / scale) in [-7, 7] (ties to even; both divisions single IEEE
+// fp32 divisions; an all-zero token gets scale 0 and codes 0), stored biased
+// as the nibbles code + 8, two per byte with the lower dim (K) or the lower
+// token (V) in the low nibble. K codes stay token-major [S][d/2]; V codes are
+// dim-major [d][S/2].
+
+namespace gqa {
+namespace decode {
+
+constexpr int kQuant4Tokens = 32;  // tokens per block; one warp per token pair at a time
+
+__global__ void __launch_bounds__(256)
+    quantize_kv_q4_kernel(const uint16_t* k, const uint16_t* v, uint8_t* kc, uint8_t* vc,
+                          float* ks, float* vs, int S) {
+    __shared__ __align__(16) uint8_t vt[128][kQuant4Tokens / 2];  // V codes, dim-major
+    const int bh = blockIdx.y, t0 = blockIdx.x * kQuant4Tokens;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int pr = warp; pr < kQuant4Tokens / 2; pr += 8) {
+        uint32_t vnib[2] = {0u, 0u};  // per token of the pair: this lane's 4 V nibbles
+        for (int h = 0; h < 2; ++h) {
+            const int t = t0 + 2 * pr + h;
+            if (t >= S) continue;  // uniform over the warp
+            const size_t row = size_t(bh) * S + t;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t* src = (which ? v : k) + row * 128;
+                const uint2 w = reinterpret_cast<const uint2*>(src)[lane];  // dims 4l .. 4l+3
+                float x[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                              __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u)};
+                float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+                amax = warp_max(amax);
+                const float sc = __fdiv_rn(amax, 7.f);
+                uint32_t nib = 0;  // nibble e = dim 4l + e
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float qv = sc > 0.f ? rintf(__fdiv_rn(x[e], sc)) : 0.f;
+                    qv = fminf(fmaxf(qv, -7.f), 7.f);
+                    nib |= uint32_t(int(qv) + 8) << (4 * e);
+                }
+                if (which == 0) {
+                    reinterpret_cast<uint16_t*>(kc + row * 64)[lane] = uint16_t(nib);
+                    if (lane == 0) ks[row] = sc;
+                } else {
+                    vnib[h] = nib;
+                    if (lane == 0) vs[row] = sc;
+                }
+            }
+        }
+        // byte pr of dim row 4l + e: token 2pr in the low nibble, 2pr + 1 high
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            vt[4 * lane + e][pr] =
+                uint8_t(((vnib[0] >> (4 * e)) & 0xFu) | (((vnib[1] >> (4 * e)) & 0xFu) << 4));
+    }
+    __syncthreads();
+    // dim-major rows: the block's 32 tokens of one dim are 16 bytes
+    for (int dim = threadIdx.x; dim < 128; dim += blockDim.x) {
+        const int nbytes = min(kQuant4Tokens, S - t0) / 2;  // S % 32 == 0: always 16
+        uint8_t* dst = vc + (size_t(bh) * 128 + dim) * (S / 2) + t0 / 2;
+        if (nbytes == kQuant4Tokens / 2)
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&vt[dim][0]);
+        else
+            for (int j = 0; j < nbytes; ++j) dst[j] = vt[dim][j];
+    }
+}
+
+}  // namespace decode
+}  // namespace gqa
+
+extern "C" int gqa_attn_quantize_kv_q4(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
+                                       uint8_t* v_codes, float* k_scales, float* v_scales, int B,
+                                       int H_kv, int S, int d, cudaStream_t stream) {
+    if (!k || !v || !k_codes || !v_codes || !k_scales || !v_scales) return GQA_ERR_INVALID_ARG;
+    if (B < 0 || H_kv <= 0 || S <= 0) return GQA_ERR_INVALID_ARG;
+    if (d != 128 || S % 32 != 0) return GQA_ERR_UNSUPPORTED;
+    if (int64_t(B) * H_kv > 65535 || int64_t(B) * H_kv * S >= (int64_t(1) << 31))
+        return GQA_ERR_UNSUPPORTED;
+    for (const void* ptr : {static_cast<const void*>(k), static_cast<const void*>(v),
+                            static_cast<const void*>(k_codes), static_cast<const void*>(v_codes),
+                            static_cast<const void*>(k_scales), static_cast<const void*>(v_scales)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return GQA_ERR_MISALIGNED;
+    if (B == 0) return GQA_OK;
+    const dim3 grid(unsigned(S / decode::kQuant4Tokens), unsigned(B * H_kv));
+    decode::quantize_kv_q4_kernel<<<grid, 256, 0, stream>>>(k, v, k_codes, v_codes, k_scales,
+                                                             v_scales, S);
+    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+extern "C" int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes,
+                                  const uint8_t* v_codes, const float* k_scales,
+                                  const float* v_scales, uint16_t* o, float* lse,
+                                  const int32_t* seqlens, int B, int H_q, int H_kv, int d,
+                                  int S_max, float scale, int num_splits, cudaStream_t stream) {
+    if (!k_scales || !v_scales) return GQA_ERR_INVALID_ARG;
+    int rc = decode::check_args(q, k_codes, v_codes, o, B, H_q, H_kv, d, S_max, scale, num_splits);
+    if (rc != GQA_OK) return rc;
+    if (d != 128 || S_max % 32 != 0) return GQA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(k_scales) | reinterpret_cast<uintptr_t>(v_scales)) & 15u)
+        return GQA_ERR_MISALIGNED;
+    if (B == 0) return GQA_OK;
+    int ns = num_splits;
+    if (ns == 0) {
+        const int sms = num_sms();
+        if (sms <= 0) return GQA_ERR_CUDA;
+        ns = gqa_attn_pick_num_splits_q4(B, H_kv, S_max, sms);
+        if (ns < 1) return GQA_ERR_INVALID_ARG;
+    }
+    const size_t bytes = decode::ws_layout(B, H_q, d, ns,
+                                           decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
+                             .total;
+    void* ws = nullptr;
+    if (bytes > 0) {
+        ws = stream_workspace(stream, bytes);
+        if (!ws) return GQA_ERR_WORKSPACE;
+    }
+    return decode::run(q, reinterpret_cast<const uint16_t*>(k_codes),
+                       reinterpret_cast<const uint16_t*>(v_codes), o, lse, seqlens, B, H_q, H_kv,
+                       d, S_max, scale, ns, ws, bytes, stream, /*ring=*/false, k_scales, v_scales,
+                       /*o32=*/nullptr, /*int4=*/true);
 }
 
 #ifdef GQA_TRACE

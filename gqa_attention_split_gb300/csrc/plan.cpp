@@ -52,6 +52,12 @@ extern "C" int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_s
     return gqa_attn_pick_num_splits(B, H_kv, int((int64_t(S_max) + 1) / 2), num_sms);
 }
 
+// An INT4 token (d code bytes + 2 fp32 scales) is about a quarter of a bf16 one.
+extern "C" int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms) {
+    if (S_max <= 0) return GQA_ERR_INVALID_ARG;
+    return gqa_attn_pick_num_splits(B, H_kv, int((int64_t(S_max) + 3) / 4), num_sms);
+}
+
 extern "C" int gqa_attn_decode_cluster_size(int B, int H_kv, int num_splits, int num_sms) {
     if (B <= 0 || H_kv <= 0 || num_splits <= 0 || num_sms <= 0) return GQA_ERR_INVALID_ARG;
     return gqa::decode_cluster_size(num_splits, int64_t(num_splits) * H_kv * B, num_sms);

@@ -248,6 +248,28 @@ __device__ __forceinline__ void u8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, u
 }
 constexpr float kQ8Offset = 1152.f;  // f16 value of a biased code minus the code
 
+// Biased int4 codes (nibbles u = x + 8) to f16 pairs, exactly, one logic op
+// per pair: nib_pair_lo puts nibbles 0 and 4 of w (bits 0-3, 16-19) into the
+// low mantissa bits of two f16 with exponent 0x64, the values 1024 + u =
+// 1032 + x; nib_pair_hi takes nibbles 1 and 5 (bits 4-7, 20-23), the values
+// 1024 + 16u = 1152 + 16x. Shifting w right by 8 reaches nibbles 2, 6 and
+// 3, 7. The caller scales the partner operand of the x16 values by 1/16 and
+// removes both offsets after the MMA.
+__device__ __forceinline__ uint32_t nib_pair_lo(uint32_t w) {
+    return (w & 0x000F000Fu) | 0x64006400u;
+}
+__device__ __forceinline__ uint32_t nib_pair_hi(uint32_t w) {
+    return (w & 0x00F000F0u) | 0x64006400u;
+}
+constexpr float kQ4OffsetLo = 1032.f;  // nib_pair_lo value minus the code
+constexpr float kQ4OffsetHi = 1152.f;  // nib_pair_hi value minus 16 x the code
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));

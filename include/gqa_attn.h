@@ -240,6 +240,37 @@ int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes, const uint8_t*
                        const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max,
                        float scale, int num_splits, cudaStream_t stream);
 
+/* ------------------------------------------------------- INT4 KV cache ----
+ * The same page and recommendation (§4 item 3), with 4-bit codes: one fp32
+ * scale per (batch row, KV head, token) for K and one for V, scale =
+ * max|x| / 7, codes rint(x / scale) in [-7, 7] (ties to even; single IEEE
+ * fp32 divisions; an all-zero token has scale 0 and codes 0). A code x is
+ * stored as the nibble x + 8, two per byte, the lower dim (K) or the lower
+ * token (V) in the low nibble. Layouts:
+ *   k_codes  uint8 [B, H_kv, S, d/2]  token-major
+ *   v_codes  uint8 [B, H_kv, d, S/2]  dim-major (V transposed)
+ *   k_scales, v_scales  fp32 [B, H_kv, S]
+ * d must be 128 and S a multiple of 32; every pointer 16-byte aligned. */
+
+/* Quantises a bf16 cache k, v [B, H_kv, S, d] into the layouts above.
+ * Async on `stream`. */
+int gqa_attn_quantize_kv_q4(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
+                            uint8_t* v_codes, float* k_scales, float* v_scales, int B, int H_kv,
+                            int S, int d, cudaStream_t stream);
+
+/* Split-KV decode over an INT4 cache: as gqa_attn_decode_q8 (num_splits == 0
+ * resolved with gqa_attn_pick_num_splits_q4). The result is attention over
+ * the dequantised cache code * scale: the kernel turns each nibble into an
+ * exact f16 value (K: 1032 + code, or 1152 + 16 x code for every second
+ * nibble; V: 1152 + 16 x code), scales the partner operand of the 16 x code
+ * values by 1/16, takes the offsets off once per head, and applies the K
+ * scale to each token's scores and the V scale to each token's softmax
+ * weight. */
+int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes, const uint8_t* v_codes,
+                       const float* k_scales, const float* v_scales, uint16_t* o, float* lse,
+                       const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max,
+                       float scale, int num_splits, cudaStream_t stream);
+
 /* --------------------------------------------------------------- prefill --
  * gqa_attn_prefill: T_q new queries at global positions q_offset + t against
  * S_kv keys (the cache already holds the new keys: q_offset + T_q <= S_kv).
@@ -280,6 +311,11 @@ int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
  * bytes, and an INT8 token (2 x d code bytes + 2 fp32 scales) is about half
  * a bf16 token (4 x d bytes). Returns >= 1, or GQA_ERR_INVALID_ARG. */
 int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_sms);
+
+/* Split count for a decode over an INT4 cache: gqa_attn_pick_num_splits for a
+ * row of ceil(S_max / 4) keys (an INT4 token, d code bytes + 2 fp32 scales,
+ * is about a quarter of a bf16 token). Returns >= 1, or GQA_ERR_INVALID_ARG. */
+int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms);
 
 /* Cluster size a decode launch uses on a GPU with num_sms SMs: the largest of
  * 16, 8, 4, 2 that divides num_splits (else 1), at most 8 when the grid of

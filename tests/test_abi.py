@@ -257,3 +257,34 @@ def test_merge_and_partial_bad_args_return_codes_without_launch(L):
                                        0.125, 0, st) == api.GQA_ERR_MISALIGNED
     assert api.gqa_attn_decode_partial(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 8, 1, 64, 256, 0.125,
                                        0, st) == 0                         # empty batch
+
+
+def test_pick_num_splits_q4_plans_a_quarter_of_the_keys(L):
+    # an INT4 token is about a quarter of the bytes of a bf16 one
+    assert api.gqa_attn_pick_num_splits_q4(1, 8, 8192, 152) == 8      # 8K decode: 1024 / split
+    assert api.gqa_attn_pick_num_splits_q4(4, 8, 131072, 152) == 32   # 128K ragged: a quarter
+    for B, H_kv, S, sms in itertools.product((1, 4, 64), (1, 8), (1, 2, 255, 513, 8192, 131072),
+                                             (1, 152)):
+        assert api.gqa_attn_pick_num_splits_q4(B, H_kv, S, sms) == \
+            _pick_reference(B, H_kv, -(-S // 4), sms), (B, H_kv, S, sms)
+    assert api.gqa_attn_pick_num_splits_q4(1, 8, 0, 152) == api.GQA_ERR_INVALID_ARG
+
+
+def test_q4_bad_args_return_codes_without_launch(L):
+    st = None
+    # k, v, k_codes, v_codes, k_scales, v_scales, B, H_kv, S, d
+    assert api.gqa_attn_quantize_kv_q4(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 1, 64, 128,
+                                       st) == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_quantize_kv_q4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 48, 128,
+                                       st) == api.GQA_ERR_UNSUPPORTED    # S % 32 != 0
+    assert api.gqa_attn_quantize_kv_q4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64,
+                                       st) == api.GQA_ERR_UNSUPPORTED    # d != 128
+    assert api.gqa_attn_quantize_kv_q4(FAKE, FAKE, FAKE + 4, FAKE, FAKE, FAKE, 1, 1, 64, 128,
+                                       st) == api.GQA_ERR_MISALIGNED
+    # q, k_codes, v_codes, k_scales, v_scales, o, lse, seqlens, B, H_q, H_kv, d, S_max, scale, ns
+    assert api.gqa_attn_decode_q4(FAKE, FAKE, FAKE, 0, FAKE, FAKE, 0, 0, 1, 8, 1, 128, 64, 0.1,
+                                  0, st) == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_decode_q4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 128, 48,
+                                  0.1, 0, st) == api.GQA_ERR_UNSUPPORTED
+    assert api.gqa_attn_decode_q4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, 8, 1, 128, 64,
+                                  0.1, 0, st) == 0                       # empty batch
