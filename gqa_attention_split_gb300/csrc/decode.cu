@@ -1113,7 +1113,10 @@ constexpr int kTileT = GQA_DEC_TILE_T, kStages = GQA_DEC_STAGES, kWarps = GQA_DE
 // stages per CTA, a longer grid 3 warps x 2 stages (GB300, 8K decode: 9.4 vs
 // 9.8 us; ragged 128K batch: 106 vs 97 us).
 constexpr int kTileTQ8 = 64;
-// int4 caches: 64 tokens per stage (8 KB of codes + 512 B of scales)
+// int4 caches: 64 tokens per stage (8 KB of codes + 512 B of scales), 4 warps x
+// 2 stages per CTA on one-wave and longer grids alike (GB300: 8K decode 9.35 us,
+// ragged 128K 80.4 us; 4 x 3: 9.39 / 81.3; 3 x 3 on the long grid: 99.7; 2 x 4:
+// 10.3 / 80.4; 6 x 2 and 8 x 1, at one CTA per SM: 15-16 / 125-134)
 constexpr int kTileTQ4 = 64;
 #ifndef GQA_DEC_Q4_WARPS
 #define GQA_DEC_Q4_WARPS 4
@@ -1121,8 +1124,14 @@ constexpr int kTileTQ4 = 64;
 #ifndef GQA_DEC_Q4_STAGES
 #define GQA_DEC_Q4_STAGES 2
 #endif
+#ifndef GQA_DEC_Q4_WARPS_MW
+#define GQA_DEC_Q4_WARPS_MW 4
+#endif
+#ifndef GQA_DEC_Q4_STAGES_MW
+#define GQA_DEC_Q4_STAGES_MW 2
+#endif
 constexpr int kQ4WarpsOneWave = GQA_DEC_Q4_WARPS, kQ4StagesOneWave = GQA_DEC_Q4_STAGES;
-constexpr int kQ4Warps = 3, kQ4Stages = 3;
+constexpr int kQ4Warps = GQA_DEC_Q4_WARPS_MW, kQ4Stages = GQA_DEC_Q4_STAGES_MW;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

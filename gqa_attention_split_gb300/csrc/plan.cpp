@@ -52,10 +52,12 @@ extern "C" int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_s
     return gqa_attn_pick_num_splits(B, H_kv, int((int64_t(S_max) + 1) / 2), num_sms);
 }
 
-// An INT4 token (d code bytes + 2 fp32 scales) is about a quarter of a bf16 one.
+// INT4 takes the INT8 rule. Its token is about a quarter of a bf16 one in
+// bytes, but the decode over it is bound by issue, not bytes, like the INT8
+// one (GB300: 8K decode 9.35 us at 16 splits vs 10.0 at 8; ragged 128K 80.4 us
+// at 64 vs 89.0 at 32).
 extern "C" int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms) {
-    if (S_max <= 0) return GQA_ERR_INVALID_ARG;
-    return gqa_attn_pick_num_splits(B, H_kv, int((int64_t(S_max) + 3) / 4), num_sms);
+    return gqa_attn_pick_num_splits_q8(B, H_kv, S_max, num_sms);
 }
 
 extern "C" int gqa_attn_decode_cluster_size(int B, int H_kv, int num_splits, int num_sms) {

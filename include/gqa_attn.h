@@ -312,9 +312,11 @@ int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
  * a bf16 token (4 x d bytes). Returns >= 1, or GQA_ERR_INVALID_ARG. */
 int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_sms);
 
-/* Split count for a decode over an INT4 cache: gqa_attn_pick_num_splits for a
- * row of ceil(S_max / 4) keys (an INT4 token, d code bytes + 2 fp32 scales,
- * is about a quarter of a bf16 token). Returns >= 1, or GQA_ERR_INVALID_ARG. */
+/* Split count for a decode over an INT4 cache: the INT8 rule,
+ * gqa_attn_pick_num_splits_q8. An INT4 token is about a quarter of a bf16 one
+ * in bytes, but both quantised decodes are bound by instruction issue rather
+ * than bytes, and measured faster with the INT8 split counts. Returns >= 1, or
+ * GQA_ERR_INVALID_ARG. */
 int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms);
 
 /* Cluster size a decode launch uses on a GPU with num_sms SMs: the largest of

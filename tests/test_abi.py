@@ -259,14 +259,14 @@ def test_merge_and_partial_bad_args_return_codes_without_launch(L):
                                        0, st) == 0                         # empty batch
 
 
-def test_pick_num_splits_q4_plans_a_quarter_of_the_keys(L):
-    # an INT4 token is about a quarter of the bytes of a bf16 one
-    assert api.gqa_attn_pick_num_splits_q4(1, 8, 8192, 152) == 8      # 8K decode: 1024 / split
-    assert api.gqa_attn_pick_num_splits_q4(4, 8, 131072, 152) == 32   # 128K ragged: a quarter
+def test_pick_num_splits_q4_takes_the_int8_rule(L):
+    # both quantised decodes are issue-bound: INT4 plans like INT8 (half the row)
+    assert api.gqa_attn_pick_num_splits_q4(1, 8, 8192, 152) == 16     # 8K decode
+    assert api.gqa_attn_pick_num_splits_q4(4, 8, 131072, 152) == 64   # 128K ragged
     for B, H_kv, S, sms in itertools.product((1, 4, 64), (1, 8), (1, 2, 255, 513, 8192, 131072),
                                              (1, 152)):
         assert api.gqa_attn_pick_num_splits_q4(B, H_kv, S, sms) == \
-            _pick_reference(B, H_kv, -(-S // 4), sms), (B, H_kv, S, sms)
+            _pick_reference(B, H_kv, -(-S // 2), sms), (B, H_kv, S, sms)
     assert api.gqa_attn_pick_num_splits_q4(1, 8, 0, 152) == api.GQA_ERR_INVALID_ARG
 
 
