@@ -72,6 +72,7 @@ struct SplitParams {
     float* part_l;            // [B, H_q, n_groups]
     unsigned* status;
     int B, H_q, H_kv, G, S_max, ns, L, n_groups;
+    int hgroups;              // CTAs per (split, KV head): 1, or 2 when G > 8 (heads in groups of 8)
     float scale_log2;         // scale * log2(e)
     int inject_timeout;       // test hook: block (0,0,0) withholds its first copy
     int trace_row0;           // first timeline row of this launch (trace builds only)
@@ -185,13 +186,19 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                  const __grid_constant__ CUtensorMap tmap_vs, const SplitParams p) {
     using C = SplitCfg<D, TILE_T, STAGES, WARPS, Q8, Q4>;
     constexpr bool kQ = C::kQuant;  // int8 or int4 codes with per-token scales
-    const int s = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+    const int s = blockIdx.x, b = blockIdx.z;
+    // KV head, and this CTA's query heads of its group: at most kMaxG, the
+    // MMA's N; a larger group runs as several CTAs over the same K/V tiles
+    const int kv = p.hgroups == 2 ? int(blockIdx.y >> 1) : int(blockIdx.y);  // 1 or 2 groups
+    const int hsub = p.hgroups == 2 ? int(blockIdx.y & 1u) : 0;
+    const int Gc = min(kMaxG, p.G - hsub * kMaxG);      // heads of this CTA
+    const int head0 = kv * p.G + hsub * kMaxG;           // its first query head
     const int gi = s / CS;         // cluster (group) index within the row
     const int rank = s % CS;       // == %cluster_ctarank for a (CS, 1, 1) cluster
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
 
-    [[maybe_unused]] const int blin = p.trace_row0 + (b * gridDim.y + kv) * gridDim.x + s;
+    [[maybe_unused]] const int blin = p.trace_row0 + (b * gridDim.y + blockIdx.y) * gridDim.x + s;
     if (threadIdx.x == 0) {
         GQA_TRACE_STAMP(blin, 0);
         unsigned smid;
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset) + warp * STAGES;
     uint8_t* ring = smem + size_t(warp) * STAGES * C::kStageBytes;
     // Heads whose cluster merge this CTA owns: h = rank, rank + CS, ... < G.
-    const int n_own = CS > 1 && rank < p.G ? (p.G - rank + CS - 1) / CS : 0;
+    const int n_own = CS > 1 && rank < Gc ? (Gc - rank + CS - 1) / CS : 0;
     float* recv = reinterpret_cast<float*>(smem + C::kRecvOffset);  // [n_own][CS][kRec]
     if (lane == 0) {
         for (int i = 0; i < STAGES; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -272,8 +279,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     // single group this can only be a row of length 0: O = 0, lse = -inf.
     if (int64_t(gi) * CS * p.L >= seqlen) {
         if (p.n_groups == 1 && rank == 0) {
-            for (int i = threadIdx.x; i < p.G * D; i += C::kThreads) {
-                const size_t row = size_t(b) * p.H_q + kv * p.G + i / D;
+            for (int i = threadIdx.x; i < Gc * D; i += C::kThreads) {
+                const size_t row = size_t(b) * p.H_q + head0 + i / D;
                 emit(p, row, 0, i % D, D, -INFINITY, 0.f, 0.f);
             }
         }
@@ -355,8 +362,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     float qsum = 0.f;
     [[maybe_unused]] float hs0 = p.scale_log2, hs1 = p.scale_log2;  // quantised: heads 2c, 2c+1
     {
-        const bool has = g < p.G;
-        const uint16_t* qh = p.q + (size_t(b) * p.H_q + kv * p.G + (has ? g : 0)) * D;
+        const bool has = g < Gc;
+        const uint16_t* qh = p.q + (size_t(b) * p.H_q + head0 + (has ? g : 0)) * D;
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qh);
         if constexpr (kQ) {
             uint2 w[C::kKC];  // dims 32c + 4j .. +3 in w[j]
@@ -937,9 +944,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
                 const int dim = md * 16 + g + (e >> 1) * 8;
                 const int head = 2 * c + (e & 1);
                 const float mm = (e & 1) ? ms1 : ms0, ll = (e & 1) ? l1 : l0;
-                if (head < p.G) {
+                if (head < Gc) {
                     if constexpr (CS == 1)
-                        emit(p, size_t(b) * p.H_q + kv * p.G + head, gi, dim, D, mm, ll,
+                        emit(p, size_t(b) * p.H_q + head0 + head, gi, dim, D, mm, ll,
                              acc[md][e]);
                     else
                         st_dsmem(rbase[e & 1] + (4 + dim) * 4, acc[md][e]);
@@ -947,11 +954,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
             }
         }
         if (CS > 1 && g == 0) {
-            if (2 * c < p.G) {
+            if (2 * c < Gc) {
                 st_dsmem(rbase[0] + 0, ms0);
                 st_dsmem(rbase[0] + 4, l0);
             }
-            if (2 * c + 1 < p.G) {
+            if (2 * c + 1 < Gc) {
                 st_dsmem(rbase[1] + 0, ms1);
                 st_dsmem(rbase[1] + 4, l1);
             }
@@ -991,7 +998,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 #pragma unroll
                     for (int e = 0; e < kPer; ++e) o[e] += fq * fv[e];
                 }
-                const size_t row = size_t(b) * p.H_q + kv * p.G + rank + j * CS;
+                const size_t row = size_t(b) * p.H_q + head0 + rank + j * CS;
 #pragma unroll
                 for (int e = 0; e < kPer; ++e) emit(p, row, gi, lane * kPer + e, D, mstar, lsum, o[e]);
             }
@@ -1135,6 +1142,13 @@ constexpr int kQ4Warps = GQA_DEC_Q4_WARPS_MW, kQ4Stages = GQA_DEC_Q4_STAGES_MW;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// CTAs of a decode launch: one per (split, KV head, batch row), times the
+// groups of at most kMaxG query heads a KV head's group splits into.
+int64_t grid_ctas(int ns, int B, int H_q, int H_kv) {
+    const int G = H_q / H_kv;
+    return int64_t(ns) * H_kv * B * ((G + kMaxG - 1) / kMaxG);
+}
+
 // Cluster size of a launch on this device (the rule is decode_cluster_size in
 // plan.cuh; ragged 128K decode on GB300: 141 us with clusters of 16, 132 us
 // with 8).
@@ -1157,6 +1171,11 @@ WsLayout ws_layout(int B, int H_q, int d, int ns, int cs) {
     w.l_off = w.m_off + align256(rows * sizeof(float));
     w.total = w.l_off + align256(rows * sizeof(float));
     return w;
+}
+
+// Workspace bytes of a launch on this device (0 when one cluster covers a row).
+size_t launch_ws_bytes(int B, int H_q, int H_kv, int d, int ns) {
+    return ws_layout(B, H_q, d, ns, cluster_size_for(ns, grid_ctas(ns, B, H_q, H_kv))).total;
 }
 
 // Cache formats of a launch: bf16 K/V, int8 codes, int4 codes.
@@ -1185,7 +1204,7 @@ int launch_split(const SplitParams& sp, const CUtensorMap (&maps)[4], cudaStream
         device_attrs_mark(attr_done, dev);
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sp.ns, sp.H_kv, sp.B);
+    cfg.gridDim = dim3(sp.ns, sp.H_kv * sp.hgroups, sp.B);
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
@@ -1265,7 +1284,8 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
     if (num_splits < 0 || num_splits > 8192) return GQA_ERR_INVALID_ARG;
     if (!isfinite(scale)) return GQA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
-    if (H_q / H_kv > kMaxG) return GQA_ERR_UNSUPPORTED;
+    if (H_q / H_kv > 2 * kMaxG) return GQA_ERR_UNSUPPORTED;
+    if (int64_t(H_kv) * ((H_q / H_kv + kMaxG - 1) / kMaxG) > 65535) return GQA_ERR_UNSUPPORTED;
     if (int64_t(B) * H_kv * S_max > (int64_t(1) << 31)) return GQA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return GQA_ERR_MISALIGNED;
@@ -1284,7 +1304,7 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     const bool q4 = k_scales != nullptr && int4;
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
-    const int cs = cluster_size_for(ns, int64_t(ns) * H_kv * B);
+    const int cs = cluster_size_for(ns, grid_ctas(ns, B, H_q, H_kv));
     const WsLayout wl = ws_layout(B, H_q, d, ns, cs);
     if (wl.total > 0) {
         if (!ws || ws_bytes < wl.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
@@ -1351,19 +1371,21 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     sp.H_q = H_q;
     sp.H_kv = H_kv;
     sp.G = H_q / H_kv;
+    sp.hgroups = (sp.G + kMaxG - 1) / kMaxG;
     sp.S_max = S_max;
     sp.ns = ns;
     sp.L = split_len(S_max, ns);
     sp.n_groups = ns / cs;
-    sp.warm_l2 = int64_t(ns) * H_kv * B <= num_sms() ? 1 : 0;  // a single wave
+    sp.warm_l2 = grid_ctas(ns, B, H_q, H_kv) <= num_sms() ? 1 : 0;  // a single wave
     sp.ring = ring ? 1 : 0;
     sp.scale_log2 = scale * kLog2e;
     sp.inject_timeout = take_injected_timeout() ? 1 : 0;
 #ifdef GQA_TRACE
     static int trace_row = 0;  // consecutive launches get consecutive timeline rows
-    if (trace_row + ns * H_kv * B > kTraceCombineBase) trace_row = 0;
+    const int nctas = int(grid_ctas(ns, B, H_q, H_kv));
+    if (trace_row + nctas > kTraceCombineBase) trace_row = 0;
     sp.trace_row0 = trace_row;
-    trace_row += ns * H_kv * B;
+    trace_row += nctas;
 #endif
     if (q8) return launch<128, kInt8>(sp, cs, maps, stream);
     if (q4) return launch<128, kInt4>(sp, cs, maps, stream);
@@ -1415,9 +1437,7 @@ extern "C" int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint1
         ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
-    const size_t bytes =
-        decode::ws_layout(B, H_q, d, ns, decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
-            .total;
+    const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
     if (bytes > 0) {
         ws = stream_workspace(stream, bytes);
@@ -1509,9 +1529,7 @@ extern "C" int gqa_attn_decode_partial(const uint16_t* q, const uint16_t* k, con
         ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
-    const size_t bytes =
-        decode::ws_layout(B, H_q, d, ns, decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
-            .total;
+    const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
     if (bytes > 0) {
         ws = stream_workspace(stream, bytes);
@@ -1611,9 +1629,7 @@ extern "C" int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const 
         ns = gqa_attn_pick_num_splits(B, H_kv, capacity, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
-    const size_t bytes = decode::ws_layout(B, H_q, d, ns,
-                                           decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
-                             .total;
+    const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
     if (bytes > 0) {
         ws = stream_workspace(stream, bytes);
@@ -1739,9 +1755,7 @@ extern "C" int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes,
         ns = gqa_attn_pick_num_splits_q8(B, H_kv, S_max, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
-    const size_t bytes = decode::ws_layout(B, H_q, d, ns,
-                                           decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
-                             .total;
+    const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
     if (bytes > 0) {
         ws = stream_workspace(stream, bytes);
@@ -1862,9 +1876,7 @@ extern "C" int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes,
         ns = gqa_attn_pick_num_splits_q4(B, H_kv, S_max, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
-    const size_t bytes = decode::ws_layout(B, H_q, d, ns,
-                                           decode::cluster_size_for(ns, int64_t(ns) * H_kv * B))
-                             .total;
+    const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
     if (bytes > 0) {
         ws = stream_workspace(stream, bytes);
@@ -1947,7 +1959,7 @@ extern "C" int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, con
         ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
         if (ns < 1) return GQA_ERR_INVALID_ARG;
     }
-    const WsLayout wl = ws_layout(B, H_q, d, ns, cluster_size_for(ns, int64_t(ns) * H_kv * B));
+    const WsLayout wl = ws_layout(B, H_q, d, ns, cluster_size_for(ns, grid_ctas(ns, B, H_q, H_kv)));
     if (wl.total > kNoAllocScratchBytes) return GQA_ERR_WORKSPACE;
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);

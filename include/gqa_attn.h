@@ -53,7 +53,7 @@ typedef struct CUstream_st* cudaStream_t;
 enum {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = -1,    /* null pointer, bad size, H_q % H_kv != 0, ... */
-    GQA_ERR_UNSUPPORTED = -2,    /* decode: d not in {64, 128} or G > 8; prefill: d != 128 */
+    GQA_ERR_UNSUPPORTED = -2,    /* decode: d not in {64, 128} or G > 16; prefill: d != 128 */
     GQA_ERR_MISALIGNED = -3,     /* a tensor pointer is not 16-byte aligned */
     GQA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
     GQA_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (device status) */
@@ -67,6 +67,10 @@ enum {
  * (seqlens == NULL: all S_max). Page: §5.2 (decode, no SP) — every past key is
  * visible, only the ragged tail is masked; G query heads are folded into the
  * matmul M dimension so each K/V tile is read once per KV head.
+ *
+ * Group size G = H_q / H_kv up to 16: a group of more than 8 query heads runs
+ * as two CTAs per (split, KV head), each folding up to 8 heads into the MMA,
+ * over the same K/V tiles (the second read mostly from L2).
  *
  * Split plan (§4 FlashDecoding split-and-combine; the page's round-robin
  * rank placement has no counterpart on one GPU): num_splits contiguous
@@ -322,6 +326,8 @@ int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms);
 /* Cluster size a decode launch uses on a GPU with num_sms SMs: the largest of
  * 16, 8, 4, 2 that divides num_splits (else 1), at most 8 when the grid of
  * num_splits * H_kv * B CTAs needs more than one wave (more CTAs than SMs).
+ * (For a group of more than 8 query heads the grid has twice that many CTAs:
+ * pass 2 * H_kv.)
  * The splits of one cluster are merged on chip; a row spanning several
  * clusters is finished by the combine kernel. Returns the size, or
  * GQA_ERR_INVALID_ARG. */

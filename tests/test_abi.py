@@ -166,7 +166,8 @@ FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case fails host che
     ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, float("nan"), 0), api.GQA_ERR_INVALID_ARG),
     # unsupported head dim / group size
     ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 96, 256, 0.125, 0), api.GQA_ERR_UNSUPPORTED),
-    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 16, 1, 64, 256, 0.125, 0), api.GQA_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 17, 1, 64, 256, 0.125, 0), api.GQA_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 32, 1, 64, 256, 0.125, 0), api.GQA_ERR_UNSUPPORTED),
     # misaligned pointer
     ((FAKE + 2, FAKE, FAKE, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, 0), api.GQA_ERR_MISALIGNED),
     ((FAKE, FAKE, FAKE + 8, FAKE, 0, 0, 1, 8, 1, 64, 256, 0.125, 0), api.GQA_ERR_MISALIGNED),

@@ -66,8 +66,9 @@ def test_tiny_decode_workload(ns):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 12, 16])
 def test_small_shapes_group_sizes(d, G):
+    # G > 8: two CTAs per (split, KV head), 8 and G - 8 heads
     H_kv = 2
     q, k, v, _ = wl.small_decode(2, H_kv * G, H_kv, d, 300, seed=100 + G + d)
     sl = torch.tensor([300, 97], dtype=torch.int32)
@@ -77,7 +78,7 @@ def test_small_shapes_group_sizes(d, G):
         assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"d={d} G={G} ns={ns}")
 
 
-@pytest.mark.parametrize("d,G", [(128, 8), (64, 4), (128, 1)])
+@pytest.mark.parametrize("d,G", [(128, 8), (64, 4), (128, 1), (128, 16), (64, 10)])
 def test_cluster_merge_every_cluster_size(d, G):
     # ns = 2, 4, 8, 16 merge one cluster per row on chip; 32, 48, 64 add the
     # cross-cluster combine; 6 and 24 use clusters of 2 and 8.

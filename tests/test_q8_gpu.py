@@ -84,7 +84,7 @@ def test_quantiser_matches_the_oracle_bit_for_bit():
     assert oks[0, 0, 5] == 1.0 and okc[0, 0, 5, 1] == 0  # rint(0.5) = 0
 
 
-@pytest.mark.parametrize("S_max,G", [(1024, 8), (3008, 4), (160, 1)])
+@pytest.mark.parametrize("S_max,G", [(1024, 8), (3008, 4), (160, 1), (1024, 16)])
 def test_decode_matches_the_oracle_on_ragged_rows(S_max, G):
     lens = sorted({0, 1, 15, 16, 17, 63, 64, 65, min(100, S_max), S_max // 2 + 3, S_max})
     B, H_kv, d = len(lens), 2, 128
