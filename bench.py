@@ -106,7 +106,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -666,8 +666,9 @@ def run_case(args):
 
         graph_calls = len(sets)
         work, unit = kv_b / 1e9, "GB/s"
-    elif args.case in ("prefill8k", "chunked32k"):
-        p = wl.CAUSAL_PREFILL_8K if args.case == "prefill8k" else wl.CHUNKED_PREFILL_32K
+    elif args.case in ("prefill8k", "chunked32k", "prefill8k_mha"):
+        p = {"prefill8k": wl.CAUSAL_PREFILL_8K, "chunked32k": wl.CHUNKED_PREFILL_32K,
+             "prefill8k_mha": wl.CAUSAL_PREFILL_8K_MHA}[args.case]
         q, k, v = (t.to(dev) for t in wl.prefill_inputs(p))
 
         def call():
@@ -725,9 +726,9 @@ def main():
                     help="CPU work per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="decode8k | ragged128k | ring8k | decode8k_q8 | ragged128k_q8 | "
-                         "decode8k_q4 | ragged128k_q4 | prefill8k | chunked32k: one workload "
-                         "alone")
+                    help="one workload alone: decode8k | ragged128k | ring8k | decode8k_q8 | "
+                         "ragged128k_q8 | decode8k_q4 | ragged128k_q4 | prefill8k | chunked32k "
+                         "| prefill8k_mha")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-worker-steps", type=int, default=1, help=argparse.SUPPRESS)

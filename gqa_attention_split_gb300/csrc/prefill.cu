@@ -8,22 +8,15 @@
 //        all-past (ke <= qs: no mask), all-future (ks >= qe: skipped) or
 //        partial (masked), in global positions (chunked prefill at q_offset).
 //
-// GB300 mapping. One CTA per work item (batch, query head, 128-row query
-// block), heaviest blocks first; the heads of one KV group are adjacent so
-// their K/V tiles are shared through L2. Six warps:
-//   warp 0   TMA producer: the Q block once, then K_j and V_j (128 keys each)
-//            into a 2-stage shared-memory ring, 128-byte swizzled.
-//   warp 1   owns the tensor memory (512 columns: S double buffer + O) and
-//            issues tcgen05.mma from one thread: S_j = Q K_j^T (both operands
-//            K-major) into S[j % 2], then O += P_{j-1} V_{j-1} (V read
-//            MN-major straight from its [keys][d] layout). S_{j} is issued
-//            before O += P_{j-1} V_{j-1} so the tensor core runs while the
-//            softmax works on S_{j-1}.
-//   warps 2-5 softmax, one query row per thread (tensor-memory lane): load the
-//            S row, mask, row max, exp2, row sum, P (bf16) into shared memory
-//            in the MMA's swizzled layout; rescale the O row in tensor memory
-//            only when the running max grows by more than 2^8 (the exps stay
-//            below 256, well inside bf16 and fp32); epilogue O / l -> bf16.
+// GB300 mapping (prefill_pair_kernel below): a persistent kernel, one CTA per
+// SM, walks work items heaviest first. A work item is two groups of 128
+// query rows that read the same K/V tiles: one query block of two heads of a
+// KV group (even G, the page's GQA lever of folding a group's heads together
+// applied to prefill), or two consecutive query blocks of one head (odd G).
+// A TMA warp streams Q and the K/V tiles, one thread issues every tcgen05.mma
+// (S = Q K^T into tensor memory, O += P V with P read from tensor memory),
+// and one softmax warpgroup per group runs the online softmax row by row
+// (one query row per thread) and the epilogue.
 // Every wait is bounded and reports a timeout in the status word.
 
 #include <cuda_runtime.h>
@@ -42,22 +35,11 @@ namespace prefill {
 constexpr int BM = kPrefillBlockM;  // 128 query rows per work item
 constexpr int BN = kPrefillBlockN;  // 128 keys per KV tile
 constexpr int D = 128;
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
 constexpr uint32_t kBoxBytes = 128 * 128;        // [128 rows][64 bf16]
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;   // [128 rows][128 bf16], two boxes
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKVOff = kTileBytes;                          // stage s: K, then V
-constexpr uint32_t kPOff = kKVOff + kStages * 2 * kTileBytes;    // P tile
-constexpr uint32_t kBarOff = kPOff + kTileBytes;
-constexpr int kSmemBytes = 1024 + kBarOff + 256;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
-constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemCols = 512;  // S_0, S_1, O_0, O_1: 128 columns each
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: rescale O when max grows by > 256x
-
-enum Bar { kQFull = 0, kKVFull = 1, kKVEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9,
-           kPVDone = 10, kMmaDrain = 11, kNumBars = 12 };
 
 struct Params {
     uint16_t* o;        // [B, H_q, T_q, D]
@@ -125,355 +107,33 @@ __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                   const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
-    auto bar = [&](int i) { return smem_u32(&bars[i]); };
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // ---- work item: heaviest query blocks first, heads of a KV group adjacent
-    const int bh_count = p.B * p.H_q;
-    const int mb = p.n_mblocks - 1 - int(blockIdx.x) / bh_count;
-    const int bh = int(blockIdx.x) % bh_count;
-    const int b = bh / p.H_q, h = bh % p.H_q, kvh = h / p.G;
-    const int m0 = mb * BM;
-    const int qs = p.q_offset + m0;                          // global query positions
-    const int qe = p.q_offset + min(m0 + BM, p.T_q);
-    int n_tiles = (p.S_kv + BN - 1) / BN;
-    if (p.causal) n_tiles = min(n_tiles, (qe - 1) / BN + 1);  // all-future tiles skipped
-
-    if (threadIdx.x == 0) {
-        mbar_init(bar(kQFull), 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(kKVFull + s), 1);
-            mbar_init(bar(kKVEmpty + s), 1);
-            mbar_init(bar(kSFull + s), 1);
-            mbar_init(bar(kSFree + s), 4);
-        }
-        mbar_init(bar(kPFull), 4);
-        mbar_init(bar(kPVDone), 1);
-        mbar_init(bar(kMmaDrain), 1);
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tc::tmem_relinquish();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmap_q);
-            tma_prefetch_desc(&tmap_k);
-            tma_prefetch_desc(&tmap_v);
-            // Test hook: block 0 withholds its Q copy, so every wait on it runs
-            // out and reports kStatusTimeout (nothing faults, nothing hangs).
-            const bool withhold = p.inject_timeout && blockIdx.x == 0;
-            const uint32_t qdst = smem_u32(smem + kQOff);
-            if (!withhold) {
-                mbar_arrive_expect_tx(bar(kQFull), kTileBytes);
-                for (int hh = 0; hh < 2; ++hh)
-                    tma_load(qdst + hh * kBoxBytes, &tmap_q, hh * 64, m0, b * p.H_q + h,
-                             bar(kQFull));
-            }
-            bool alive = true;
-            int issued = 0;
-            for (int j = 0; j < n_tiles && alive; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages)
-                    alive = mbar_wait_bounded(bar(kKVEmpty + s), ((j / kStages) - 1) & 1, p.status);
-                if (!alive) break;
-                const uint32_t kdst = smem_u32(smem + kKVOff + s * 2 * kTileBytes);
-                const uint32_t vdst = kdst + kTileBytes;
-                mbar_arrive_expect_tx(bar(kKVFull + s), 2 * kTileBytes);
-                for (int hh = 0; hh < 2; ++hh) {
-                    tma_load(kdst + hh * kBoxBytes, &tmap_k, hh * 64, j * BN, b * p.H_kv + kvh,
-                             bar(kKVFull + s));
-                    tma_load(vdst + hh * kBoxBytes, &tmap_v, hh * 64, j * BN, b * p.H_kv + kvh,
-                             bar(kKVFull + s));
-                }
-                issued = j + 1;
-            }
-            // Never leave with copies in flight into this CTA's shared memory.
-            if (!withhold) mbar_wait_bounded(bar(kQFull), 0, p.status);
-            for (int j = max(0, issued - kStages); j < issued; ++j)
-                mbar_wait_bounded(bar(kKVFull + j % kStages), (j / kStages) & 1, p.status);
-        }
-    } else if (warp == 1) {
-        // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false);
-            const uint32_t idesc_pv = tc::idesc_bf16_f32(BM, D, true);
-            const uint32_t qsm = smem_u32(smem + kQOff), psm = smem_u32(smem + kPOff);
-            // Descriptors are built once per operand; each k-step adds its byte
-            // offset >> 4 to the start-address field of the low word (shared
-            // addresses stay below 256 KB, so the field never carries out).
-            const uint64_t qdesc = tc::sdesc_sw128(qsm, 16, 1024);
-            const uint64_t pdesc = tc::sdesc_sw128(psm, 16, 1024);
-            const uint32_t qlo = uint32_t(qdesc), qhi = uint32_t(qdesc >> 32);
-            const uint32_t plo = uint32_t(pdesc), phi = uint32_t(pdesc >> 32);
-            GQA_DBG(unsigned long long dbg[3] = {0, 0, 0};)
-            bool alive = mbar_wait_bounded(bar(kQFull), 0, p.status);
-            for (int j = 0; j <= n_tiles && alive; ++j) {
-                if (j < n_tiles) {
-                    const int s = j % kStages;
-                    alive = mbar_wait_bounded(bar(kKVFull + s), (j / kStages) & 1, p.status);
-                    if (alive && j >= 2)
-                        alive = mbar_wait_bounded(bar(kSFree + (j & 1)), ((j >> 1) - 1) & 1,
-                                                  p.status);
-                    if (!alive) break;
-                    tc::fence_after_sync();
-                    const uint32_t ksm = smem_u32(smem + kKVOff + s * 2 * kTileBytes);
-                    const uint64_t kdesc = tc::sdesc_sw128(ksm, 16, 1024);
-                    const uint32_t klo = uint32_t(kdesc), khi = uint32_t(kdesc >> 32);
-                    const uint32_t dst = tmem + (j & 1) * BN;
-                    mma_ss_lo<0>(dst, qlo, qhi, klo, khi, idesc_s);
-#pragma unroll
-                    for (int kk = 1; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-                        mma_ss_lo<1>(dst, qlo + off, qhi, klo + off, khi, idesc_s);
-                    }
-                    tc::commit(bar(kSFull + (j & 1)));
-                    GQA_DBG(dbg_count_tile(dbg, p, qs, qe, j, 1);)
-                }
-                if (j >= 1) {
-                    const int jp = j - 1, s = jp % kStages;
-                    alive = mbar_wait_bounded(bar(kPFull), jp & 1, p.status);
-                    if (!alive) break;
-                    tc::fence_after_sync();
-                    const uint32_t vsm = smem_u32(smem + kKVOff + s * 2 * kTileBytes + kTileBytes);
-                    const uint64_t vdesc = tc::sdesc_sw128(vsm, kBoxBytes, 1024);
-                    const uint32_t vlo = uint32_t(vdesc), vhi = uint32_t(vdesc >> 32);
-                    if (jp > 0)
-                        mma_ss_lo<1>(tmem + kTmemO, plo, phi, vlo, vhi, idesc_pv);
-                    else
-                        mma_ss_lo<0>(tmem + kTmemO, plo, phi, vlo, vhi, idesc_pv);
-#pragma unroll
-                    for (int ks = 1; ks < BN / 16; ++ks) {
-                        const uint32_t aoff = ((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4;
-                        mma_ss_lo<1>(tmem + kTmemO, plo + aoff, phi, vlo + ((ks * 2048) >> 4), vhi,
-                                     idesc_pv);
-                    }
-                    tc::commit(bar(kPVDone));
-                    tc::commit(bar(kKVEmpty + s));
-                }
-            }
-            GQA_DBG(dbg_flush_tiles(dbg);)
-            // No MMA may still be running when the tensor memory is freed.
-            tc::commit(bar(kMmaDrain));
-            mbar_wait_bounded(bar(kMmaDrain), 0, p.status);
-        }
-    } else {
-        // ------------------------------------------------- softmax warpgroup
-        const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31
-        const int row = quad * 32 + lane;     // query row within the block
-        const int qg = qs + row;              // its global position
-        const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
-        uint8_t* psm = smem + kPOff;
-        // l_run: sum of the fp32 probabilities (for lse); lb_run: sum of the
-        // bf16-rounded probabilities the P.V MMA actually consumed, so that
-        // O / lb_run is an exact convex combination of V rows.
-        float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
-        bool alive = true;
-        for (int j = 0; j < n_tiles && alive; ++j) {
-            alive = mbar_wait_bounded(bar(kSFull + (j & 1)), (j >> 1) & 1, p.status);
-            alive = __all_sync(0xffffffffu, alive);
-            if (!alive) break;
-            tc::fence_after_sync();
-            float sv[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32(lane_base + (j & 1) * BN + c * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[i]);
-            }
-            tc::tmem_wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kSFree + (j & 1)));  // S buffer may be rewritten
-
-            // mask the boundary tile (raw scores), row max as a shallow tree
-            const int ks = j * BN, ke = min(ks + BN, p.S_kv);
-            const bool masked =
-                (p.causal && tile_class(qs, qe, ks, ke) == kTilePartial) || (ke - ks < BN);
-            if (masked) {
-                const int lim = (p.causal ? min(qg, p.S_kv - 1) : p.S_kv - 1) - ks;
-#pragma unroll
-                for (int c = 0; c < BN; ++c) sv[c] = c <= lim ? sv[c] : -INFINITY;
-            }
-            float mx;
-            {
-                float mm[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mm[i] = fmaxf(sv[i], sv[8 + i]);
-#pragma unroll
-                for (int c = 16; c < BN; c += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mm[i] = fmax3(mm[i], sv[c + i], sv[c + 8 + i]);
-                mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]),
-                           fmaxf(mm[6], mm[7]));
-            }
-            // scale > 0, so the max of the scaled scores is the scaled max
-            const float m_new = fmaxf(m_run, mx * p.scale_log2);
-            const bool need = m_new > m_run + kRescaleThreshold;  // true while m_run = -inf
-            const float corr = need ? fast_exp2(m_run - m_new) : 1.f;
-            const float m_use = need ? m_new : m_run;
-            m_run = m_use;
-
-            // p = 2^(s*scale - m) in packed pairs, the row sums of p (fp32) and of
-            // the bf16-rounded p, and P packed to bf16. Four independent pair
-            // accumulators keep the dependency chains short.
-            uint32_t pk[BN / 2];
-            {
-                const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
-                const uint64_t n2 = f2pack(-m_use, -m_use);
-                uint64_t s2[4];
-                float bl[4], bh[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    s2[u] = 0ull;
-                    bl[u] = bh[u] = 0.f;
-                }
-#pragma unroll
-                for (int i = 0; i < BN / 2; ++i) {
-                    float x0, x1;
-                    f2unpack(ffma2(f2pack(sv[2 * i], sv[2 * i + 1]), c2, n2), x0, x1);
-                    const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-                    s2[i & 3] = fadd2(s2[i & 3], f2pack(e0, e1));
-                    pk[i] = pack_bf16x2(e0, e1);
-                    bl[i & 3] = add_f32_bf16_lo(bl[i & 3], pk[i]);
-                    bh[i & 3] = add_f32_bf16_hi(bh[i & 3], pk[i]);
-                }
-                float t[8], tb[8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    f2unpack(s2[u], t[2 * u], t[2 * u + 1]);
-                    tb[2 * u] = bl[u];
-                    tb[2 * u + 1] = bh[u];
-                }
-                const float rs = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
-                const float rsb =
-                    ((tb[0] + tb[1]) + (tb[2] + tb[3])) + ((tb[4] + tb[5]) + (tb[6] + tb[7]));
-                l_run = l_run * corr + rs;
-                lb_run = lb_run * corr + rsb;
-            }
-
-            // P and O are free once the previous tile's P.V has completed.
-            if (j >= 1) {
-                alive = mbar_wait_bounded(bar(kPVDone), (j - 1) & 1, p.status);
-                alive = __all_sync(0xffffffffu, alive);
-                if (!alive) break;
-                tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, need)) {
-                    const uint64_t corr2 = f2pack(corr, corr);
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tc::tmem_ld32(lane_base + kTmemO + c * 32, r);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float a0, a1;
-                            f2unpack(fmul2(f2pack(__uint_as_float(r[2 * i]),
-                                                  __uint_as_float(r[2 * i + 1])),
-                                           corr2),
-                                     a0, a1);
-                            r[2 * i] = __float_as_uint(a0);
-                            r[2 * i + 1] = __float_as_uint(a1);
-                        }
-                        tc::tmem_st32(lane_base + kTmemO + c * 32, r);
-                    }
-                    tc::tmem_wait_st();
-                }
-            }
-            // P row -> shared memory in the 128-byte swizzled K-major layout
-#pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16)
-                *reinterpret_cast<uint4*>(psm + (c16 >> 3) * kBoxBytes + swz128(row, c16 & 7)) =
-                    make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-            fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async proxy
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kPFull));
-        }
-
-        // ---- epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
-        if (alive) alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kPVDone),
-                                                                      (n_tiles - 1) & 1, p.status));
-        if (alive) {
-            tc::fence_after_sync();
-            const bool valid = m0 + row < p.T_q;
-            const float inv = 1.f / lb_run;
-            const size_t orow = (size_t(b) * p.H_q + h) * p.T_q + m0 + row;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32(lane_base + kTmemO + c * 32, r);
-                tc::tmem_wait_ld();
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + c * 32);
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv,
-                                          __uint_as_float(r[v4 * 8 + 7]) * inv);
-                        dst[v4] = w;
-                    }
-                }
-            }
-            if (valid && p.lse) p.lse[orow] = (m_run + __log2f(l_run)) * kLn2;
-        }
-    }
-
-    tc::fence_before_sync();
-    __syncthreads();
-    if (warp == 1) {
-        tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
 // ---------------------------------------------------------------------------
-// Two query heads of one KV group per work item (used when G is even). The
-// page's GQA lever (§5.2, fold the G heads into the matmul M dimension)
-// applied to prefill: every K/V tile loaded into shared memory serves 2 x 128
-// query rows. P stays in tensor memory (written over its own S columns) and
-// feeds the P.V MMA as the A operand, so shared memory only carries Q, K, V.
+// The prefill kernel. A work item is two groups of 128 query rows that read
+// the same K/V tiles: with an even G, one query block of two query heads of a
+// KV group (the page's GQA lever, §5.2, fold the G heads into the matmul M
+// dimension, applied to prefill); with an odd G, two consecutive query blocks
+// of one head. Every K/V tile loaded into shared memory serves 2 x 128 query
+// rows. P stays in tensor memory (written over its own S columns) and feeds the
+// P.V MMA as the A operand, so shared memory only carries Q, K, V.
 //
 // Persistent: one CTA per SM walks the work items heaviest first (snake order
 // over the CTAs), so the next item's Q load and first S overlap the previous
 // item's epilogue, and the tensor memory is allocated once.
-//   warpgroup 0 (104 registers/thread): warp 0 TMA (per item: Q of both heads,
-//               then K_j, V_j through a 4-slot ring); warp 1 owns the tensor
-//               memory and one thread of it issues every MMA, per KV tile j:
-//               PV_A(j), S_A(j+1), PV_B(j), S_B(j+1). An S MMA overwrites the
-//               P the previous PV of its head read; the tcgen05.mma operations
-//               of one thread execute and complete in issue order. Warps 2
-//               and 3 only wait.
-//   warpgroups 1 and 2 (200 registers/thread): softmax of head A and of
-//               head B, then that head's epilogue (O through TMA stores);
+//   warpgroup 0 (104 registers/thread): warp 0 TMA (per item: Q of both
+//               groups, then K_j, V_j through a 4-slot ring); warp 1 owns the
+//               tensor memory and one thread of it issues every MMA, per KV
+//               tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), each only while
+//               its group has tiles (the groups of a block pair have different
+//               causal extents). An S MMA overwrites the P the previous PV of
+//               its group read; the tcgen05.mma operations of one thread
+//               execute and complete in issue order. Warps 2 and 3 only wait.
+//   warpgroups 1 and 2 (200 registers/thread): softmax of group A and of
+//               group B, then that group's epilogue (O through TMA stores);
 //               while one group computes, the tensor core runs the other
 //               group's MMAs.
 // Register split: 128 x 104 + 256 x 200 = 64512 = 384 threads x 168 at launch.
 // Every barrier phase is counted across items: the k-th completion of a
-// barrier has parity k & 1.
+// barrier has parity k & 1 (per group for the S, P and O barriers).
 
 constexpr int kPairThreads = 384;
 // Four 32 KB slots: ring item r (K_j or V_j of some work item) reuses the
@@ -490,13 +150,12 @@ constexpr uint32_t kStageBoxBytes = 32 * 32 * 2;
 constexpr uint32_t kPairBarOff = kPairStageOff + 8 * 2 * kStageBoxBytes;
 constexpr int kPairSmemBytes = 1024 + kPairBarOff + 256;
 static_assert(kPairSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
-static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
 // S_g (and P_g over its first 64 columns) at g*128; O_g at 256 + g*128.
 __device__ __forceinline__ uint32_t col_s_of(int g) { return uint32_t(g) * 128u; }
 __device__ __forceinline__ uint32_t col_o_of(int g) { return 256u + uint32_t(g) * 128u; }
 
 enum PairBar {
-    pQFull = 0,                        // Q of both heads landed (per item)
+    pQFull = 0,                        // Q of both groups landed (per item)
     pQEmpty = 1,                       // the item's last S MMAs have completed
     pSlotFull = 2,                     // x kRingSlots
     pSlotEmpty = pSlotFull + kRingSlots,  // x kRingSlots, released by the MMA thread's commits
@@ -508,40 +167,72 @@ enum PairBar {
 };
 static_assert(pNumBars * 8 + 4 <= 256, "barrier area");
 
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// One work item: a 128-row query block of two adjacent query heads of one
-// KV group. Items are numbered heaviest first (query blocks from the last
-// one down), and a CTA takes items c, 2G-1-c, 2G+c, ... (snake order).
+// One work item: two groups of 128 query rows that read the same K/V tiles.
+// Even G: one query block of two adjacent query heads of a KV group. Odd G
+// (pair_blocks): two consecutive query blocks of one head. Items are numbered
+// heaviest first (query blocks from the last one down), and a CTA takes items
+// c, 2G-1-c, 2G+c, ... (snake order). Each group has its own KV tile count
+// (causal: up to its own last query), possibly 0 (the second block of a head
+// with an odd block count); the item runs the larger one.
 struct PairItem {
-    int b, h0, kvh, m0, qs, qe, n_tiles;
+    int b, kvh;
+    int head[2];   // query head of group g
+    int row0[2];   // first query row of group g (row0 >= T_q: an empty group)
+    int qs[2];     // global position of that row
+    int qe[2];     // one past the group's last query (global); qe <= qs when empty
+    int n[2];      // KV tiles of group g
+    int n_tiles;   // max(n[0], n[1])
+    // (head pairs set only the [0] fields and n_tiles: head[1] = head[0] + 1,
+    // the rest equal)
 };
 
+// kBlocks: the groups are two query blocks of one head (odd G), else one
+// block of two heads (even G; then both groups share row0, qs, qe and n).
+template <bool kBlocks>
 __device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) {
     const int G = gridDim.x, c = blockIdx.x;
     const int L = it * G + ((it & 1) ? G - 1 - c : c);
-    const int pairs = p.H_q / 2, bp_count = p.B * pairs;
-    if (L >= p.n_mblocks * bp_count) return false;
-    const int mb = p.n_mblocks - 1 - L / bp_count, bp = L % bp_count;
-    w.b = bp / pairs;
-    w.h0 = (bp % pairs) * 2;
-    w.kvh = w.h0 / p.G;
-    w.m0 = mb * BM;
-    w.qs = p.q_offset + w.m0;
-    w.qe = p.q_offset + min(w.m0 + BM, p.T_q);
-    w.n_tiles = (p.S_kv + BN - 1) / BN;
-    if (p.causal) w.n_tiles = min(w.n_tiles, (w.qe - 1) / BN + 1);  // all-future tiles skipped
+    int h;
+    if constexpr (kBlocks) {
+        const int tiles = (p.S_kv + BN - 1) / BN;
+        int mb[2];
+        const int n_bpairs = (p.n_mblocks + 1) / 2, bh_count = p.B * p.H_q;
+        if (L >= n_bpairs * bh_count) return false;
+        const int bpi = n_bpairs - 1 - L / bh_count, bh = L % bh_count;
+        w.b = bh / p.H_q;
+        h = bh % p.H_q;
+        w.head[0] = w.head[1] = h;
+        mb[0] = 2 * bpi;
+        mb[1] = 2 * bpi + 1;
+        w.kvh = h / p.G;
+        for (int g = 0; g < 2; ++g) {
+            w.row0[g] = mb[g] * BM;
+            w.qs[g] = p.q_offset + w.row0[g];
+            w.qe[g] = p.q_offset + min(w.row0[g] + BM, p.T_q);
+            int n = w.row0[g] < p.T_q ? tiles : 0;
+            if (p.causal && n > 0) n = min(n, (w.qe[g] - 1) / BN + 1);  // all-future tiles skipped
+            w.n[g] = n;
+        }
+        w.n_tiles = max(w.n[0], w.n[1]);
+    } else {
+        const int pairs = p.H_q / 2, bp_count = p.B * pairs;
+        if (L >= p.n_mblocks * bp_count) return false;
+        const int m = p.n_mblocks - 1 - L / bp_count, bp = L % bp_count;
+        // only the [0] fields and n_tiles: head pairs never read the others
+        w.b = bp / pairs;
+        h = (bp % pairs) * 2;
+        w.head[0] = h;
+        w.kvh = h / p.G;
+        w.row0[0] = m * BM;
+        w.qs[0] = p.q_offset + m * BM;
+        w.qe[0] = p.q_offset + min(m * BM + BM, p.T_q);
+        w.n_tiles = (p.S_kv + BN - 1) / BN;
+        if (p.causal) w.n_tiles = min(w.n_tiles, (w.qe[0] - 1) / BN + 1);  // all-future skipped
+    }
     return true;
 }
 
+template <bool kBlocks>
 __global__ void __launch_bounds__(kPairThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
@@ -591,18 +282,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         bool alive = true;
         int r = 0;        // ring items issued so far, over all work items
         int q_loads = 0;  // Q loads issued (one per work item)
-        for (int it = 0; alive && pair_item(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks>(p, it, w); ++it) {
             // Q of both heads; the previous item's last S MMAs must be done.
             if (it > 0) alive = mbar_wait_bounded(bar(pQEmpty), (it - 1) & 1, p.status);
             if (!alive) break;
             // Test hook: block 0 withholds its first Q copy, so every wait on
             // it runs out and reports kStatusTimeout (nothing faults or hangs).
             if (!(p.inject_timeout && blockIdx.x == 0 && it == 0)) {
+                // (an empty group's rows lie past T_q: the copy reads zero fill)
                 mbar_arrive_expect_tx(bar(pQFull), 2 * kTileBytes);
                 for (int g = 0; g < 2; ++g)
                     for (int hh = 0; hh < 2; ++hh)
                         tma_load(smem_u32(smem + kPairQOff + g * kTileBytes) + hh * kBoxBytes,
-                                 &tmap_q, hh * 64, w.m0, w.b * p.H_q + w.h0 + g, bar(pQFull));
+                                 &tmap_q, hh * 64, kBlocks ? w.row0[g] : w.row0[0],
+                                 w.b * p.H_q + (kBlocks ? w.head[g] : w.head[0] + g),
+                                 bar(pQFull));
                 q_loads = it + 1;
             }
             for (int i = 0; i < 2 * w.n_tiles; ++i, ++r) {  // K_0, V_0, K_1, V_1, ...
@@ -665,49 +359,98 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 mma_ts_lo(dst, src + ks * 8, vlo + uint32_t((ks * 2048) >> 4), vhi, idesc_pv, 1u);
         };
         bool alive = true;
-        int r = 0;   // ring items consumed so far
-        int tt = 0;  // KV tiles finished so far (S and P barrier phases)
+        int r = 0;                // ring items consumed so far
+        int tt[2] = {0, 0};       // KV tiles group g finished so far (its S and P phases)
         GQA_DBG(unsigned long long dbg[3] = {0, 0, 0};)
-        for (int it = 0; alive && pair_item(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks>(p, it, w); ++it) {
             const int n = w.n_tiles;
             alive = mbar_wait_bounded(bar(pQFull), it & 1, p.status) && wait_item(r);
             if (!alive) break;
             tc::fence_after_sync();
-            issue_s(0, r);
-            issue_s(1, r);
-            GQA_DBG(dbg_count_tile(dbg, p, w.qs, w.qe, 0, 2);)
-            tc::commit(bar(pSlotEmpty + r % kRingSlots));  // K_0 read by both S MMAs
-            if (n == 1) tc::commit(bar(pQEmpty));
-            for (int j = 0; j < n && alive; ++j) {
-                const bool more = j + 1 < n;
-                const int rv = r + 2 * j + 1;  // V_j; K_{j+1} follows it
-                // the loads first (they land early), so that once P is ready
-                // only the fence and the issue remain
-                alive = wait_item(rv);
-                if (alive && more) alive = wait_item(rv + 1);
-                for (int g = 0; g < 2 && alive; ++g) {
-                    // P_g(0) of an item is written after the softmax threads
-                    // have read the previous item's O_g, so PV_g(0) may
-                    // overwrite it.
-                    alive = mbar_wait_bounded(bar(pPFull + g), (tt + j) & 1, p.status);
-                    if (!alive) break;
-                    tc::fence_after_sync();
-                    issue_pv(g, rv, j == 0);
-                    if (g == 1) tc::commit(bar(pSlotEmpty + rv % kRingSlots));  // done with V_j
-                    if (more) {
-                        issue_s(g, rv + 1);
-                        GQA_DBG(dbg_count_tile(dbg, p, w.qs, w.qe, j + 1, 1);)
-                        if (g == 1) {
-                            tc::commit(bar(pSlotEmpty + (rv + 1) % kRingSlots));  // K_{j+1}
-                            if (j + 2 == n) tc::commit(bar(pQEmpty));  // last S of the item
+            if constexpr (!kBlocks) {
+                // two heads, one query block: both groups run every tile
+                issue_s(0, r);
+                issue_s(1, r);
+                GQA_DBG(dbg_count_tile(dbg, p, w.qs[0], w.qe[0], 0, 2);)
+                tc::commit(bar(pSlotEmpty + r % kRingSlots));  // K_0 read by both S MMAs
+                if (n == 1) tc::commit(bar(pQEmpty));
+                for (int j = 0; j < n && alive; ++j) {
+                    const bool more = j + 1 < n;
+                    const int rv = r + 2 * j + 1;  // V_j; K_{j+1} follows it
+                    // the loads first (they land early), so that once P is ready
+                    // only the fence and the issue remain
+                    alive = wait_item(rv);
+                    if (alive && more) alive = wait_item(rv + 1);
+                    for (int g = 0; g < 2 && alive; ++g) {
+                        // P_g(0) of an item is written after the softmax threads
+                        // have read the previous item's O_g, so PV_g(0) may
+                        // overwrite it.
+                        alive = mbar_wait_bounded(bar(pPFull + g), (tt[0] + j) & 1, p.status);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                        issue_pv(g, rv, j == 0);
+                        if (g == 1) tc::commit(bar(pSlotEmpty + rv % kRingSlots));  // V_j done
+                        if (more) {
+                            issue_s(g, rv + 1);
+                            GQA_DBG(dbg_count_tile(dbg, p, w.qs[0], w.qe[0], j + 1, 1);)
+                            if (g == 1) {
+                                tc::commit(bar(pSlotEmpty + (rv + 1) % kRingSlots));  // K_{j+1}
+                                if (j + 2 == n) tc::commit(bar(pQEmpty));  // last S of the item
+                            }
+                        } else {
+                            tc::commit(bar(pODone + g));
                         }
-                    } else {
-                        tc::commit(bar(pODone + g));
                     }
                 }
+                tt[0] += n;
+                tt[1] += n;
+            } else {
+                // two query blocks of one head: group g runs its own n[g] tiles
+                // (possibly 0). The last group that reads K_t / V_t (t < n) is
+                // group 1 while it has tiles, else group 0.
+                auto last_user = [&](int t) { return t < w.n[1] ? 1 : 0; };
+                if (w.n[0] > 0) {
+                    issue_s(0, r);
+                    GQA_DBG(dbg_count_tile(dbg, p, w.qs[0], w.qe[0], 0, 1);)
+                }
+                if (w.n[1] > 0) {
+                    issue_s(1, r);
+                    GQA_DBG(dbg_count_tile(dbg, p, w.qs[1], w.qe[1], 0, 1);)
+                }
+                tc::commit(bar(pSlotEmpty + r % kRingSlots));  // K_0 read by the S MMAs
+                if (n == 1) tc::commit(bar(pQEmpty));
+                for (int j = 0; j < n && alive; ++j) {
+                    const int rv = r + 2 * j + 1;  // V_j; K_{j+1} follows it
+                    alive = wait_item(rv);
+                    if (alive && j + 1 < n) alive = wait_item(rv + 1);
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        if (!alive) break;
+                        const int n_g = g ? w.n[1] : w.n[0];
+                        if (j >= n_g) continue;  // this group has no tile j
+                        alive = mbar_wait_bounded(bar(pPFull + g),
+                                                  ((g ? tt[1] : tt[0]) + j) & 1, p.status);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                        issue_pv(g, rv, j == 0);
+                        if (g == last_user(j)) tc::commit(bar(pSlotEmpty + rv % kRingSlots));
+                        if (j + 1 < n_g) {
+                            issue_s(g, rv + 1);
+                            GQA_DBG(dbg_count_tile(dbg, p, g ? w.qs[1] : w.qs[0],
+                                                   g ? w.qe[1] : w.qe[0], j + 1, 1);)
+                            if (g == last_user(j + 1)) {
+                                tc::commit(bar(pSlotEmpty + (rv + 1) % kRingSlots));  // K_{j+1}
+                                if (j + 2 == n) tc::commit(bar(pQEmpty));  // last S of the item
+                            }
+                        } else {
+                            tc::commit(bar(pODone + g));
+                        }
+                    }
+                }
+                tt[0] += w.n[0];
+                tt[1] += w.n[1];
             }
             r += 2 * n;
-            tt += n;
         }
         GQA_DBG(dbg_flush_tiles(dbg);)
         // No MMA may still run when the tensor memory is freed.
@@ -717,7 +460,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
         // ------------------------------------------------ softmax warpgroups
-        const int g = wg - 1;                 // 0: head h0, 1: head h0 + 1
+        const int g = wg - 1;                 // the item's group 0 or 1
         const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
@@ -725,11 +468,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const uint32_t stage = smem_u32(smem + kPairStageOff + (g * 4 + quad) * 2 * kStageBoxBytes);
         const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
         bool alive = true;
-        int tt = 0;  // KV tiles finished so far, over all work items
-        for (int it = 0; alive && pair_item(p, it, w); ++it) {
-            const int qg = w.qs + row;
+        int tt = 0;   // KV tiles this group finished so far, over all work items
+        [[maybe_unused]] int itg = 0;  // block pairs: items in which this group had tiles
+        for (int it = 0; alive && pair_item<kBlocks>(p, it, w); ++it) {
+            // this group's fields (selected, not indexed: they stay in registers)
+            const int ng = kBlocks ? (g ? w.n[1] : w.n[0]) : w.n_tiles;
+            if constexpr (kBlocks) {
+                if (ng == 0) continue;  // an empty group (past the last query): no MMAs
+            }
+            const int qs_g = kBlocks && g ? w.qs[1] : w.qs[0];
+            const int qe_g = kBlocks && g ? w.qe[1] : w.qe[0];
+            const int qg = qs_g + row;
             float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
-            for (int j = 0; j < w.n_tiles && alive; ++j) {
+            for (int j = 0; j < ng && alive; ++j) {
                 alive = __all_sync(0xffffffffu,
                                    mbar_wait_bounded(bar(pSFull + g), (tt + j) & 1, p.status));
                 if (!alive) break;
@@ -746,7 +497,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
                 const int ks = j * BN, ke = min(ks + BN, p.S_kv);
                 const bool masked =
-                    (p.causal && tile_class(w.qs, w.qe, ks, ke) == kTilePartial) || (ke - ks < BN);
+                    (p.causal && tile_class(qs_g, qe_g, ks, ke) == kTilePartial) ||
+                    (ke - ks < BN);
                 if (masked) {
                     const int lim = (p.causal ? min(qg, p.S_kv - 1) : p.S_kv - 1) - ks;
 #pragma unroll
@@ -841,12 +593,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // ---- epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2. Every
             // read of O_g completes (wait::ld) before this warp's next P
             // arrive, which is what lets the next item's PV_g(0) overwrite O_g.
-            alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pODone + g), it & 1, p.status));
+            alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pODone + g),
+                                                              (kBlocks ? itg : it) & 1, p.status));
             if (!alive) break;
             tc::fence_after_sync();
-            const bool valid = w.m0 + row < p.T_q;
+            const int row0_g = kBlocks && g ? w.row0[1] : w.row0[0];
+            const int head_g = kBlocks ? w.head[0] : w.head[0] + g;
+            const bool valid = row0_g + row < p.T_q;
             const float inv = 1.f / lb_run;
-            const size_t orow = (size_t(w.b) * p.H_q + w.h0 + g) * p.T_q + w.m0 + row;
+            const size_t orow = (size_t(w.b) * p.H_q + head_g) * p.T_q + row0_g + row;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -873,13 +628,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     // rows at or past T_q fall outside the tensor and are not written
-                    tma_store_3d(&tmap_o, buf, c * 32, w.m0 + quad * 32,
-                                 w.b * p.H_q + w.h0 + g);
+                    tma_store_3d(&tmap_o, buf, c * 32, row0_g + quad * 32, w.b * p.H_q + head_g);
                     bulk_commit_group();
                 }
             }
             if (valid && p.lse) p.lse[orow] = (m_run + __log2f(l_run)) * kLn2;
-            tt += w.n_tiles;
+            tt += ng;
+            if constexpr (kBlocks) ++itg;
         }
         // the O stores finish before the CTA (and its shared memory) does
         if (lane == 0) bulk_wait_group_all();
@@ -949,32 +704,37 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     prm.n_mblocks = (T_q + BM - 1) / BM;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.inject_timeout = take_injected_timeout() ? 1 : 0;
+    // Even group sizes pair two heads of a KV group per work item; odd ones pair
+    // two consecutive query blocks of one head.
+    const bool blocks = prm.G % 2 != 0;
     static std::atomic<uint64_t> attr_done{0};  // once per device
     const int dev = current_device();
     if (device_attrs_pending(attr_done, dev)) {
-        if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_pair_kernel,
+        if (cudaFuncSetAttribute(prefill_pair_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_pair_kernel<true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairSmemBytes) != cudaSuccess)
             return GQA_ERR_CUDA;
         device_attrs_mark(attr_done, dev);
     }
-    // Even group sizes run two heads of a KV group per CTA; odd ones one head.
-    const bool pair = prm.G % 2 == 0;
-    const int64_t items = int64_t(prm.n_mblocks) * B * (pair ? H_q / 2 : H_q);
+    const int64_t items = blocks ? int64_t((prm.n_mblocks + 1) / 2) * B * H_q
+                                 : int64_t(prm.n_mblocks) * B * (H_q / 2);
     if (items > 0x7fffffff) return GQA_ERR_UNSUPPORTED;
-    if (pair) {
-        // persistent: one CTA per SM (at most one per work item)
-        const int ctas = int(items < int64_t(num_sms()) ? items : int64_t(num_sms()));
-        if (encode_tmap_3d_bf16(&to, o, D, T_q, uint64_t(B) * H_q, 32, 32,
-                                CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess)
-            return GQA_ERR_CUDA;
-        prefill_pair_kernel<<<dim3(unsigned(ctas)), kPairThreads, kPairSmemBytes, stream>>>(
+    // persistent: one CTA per SM (at most one per work item)
+    const int sms = num_sms();
+    if (sms <= 0) return GQA_ERR_CUDA;
+    const int ctas = int(items < int64_t(sms) ? items : int64_t(sms));
+    if (encode_tmap_3d_bf16(&to, o, D, T_q, uint64_t(B) * H_q, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    if (blocks)
+        prefill_pair_kernel<true><<<dim3(unsigned(ctas)), kPairThreads, kPairSmemBytes, stream>>>(
             tq, tk, tv, to, prm);
-    }
     else
-        prefill_kernel<<<dim3(unsigned(items)), kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
+        prefill_pair_kernel<false><<<dim3(unsigned(ctas)), kPairThreads, kPairSmemBytes,
+                                     stream>>>(tq, tk, tv, to, prm);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;
 }

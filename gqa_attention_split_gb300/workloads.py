@@ -63,6 +63,11 @@ CAUSAL_PREFILL_8K = PrefillWorkload("llama70b_causal_prefill_b1_t8192", 1, 64, 8
 CHUNKED_PREFILL_32K = PrefillWorkload("llama70b_chunked_prefill_b2_t2048_off30720", 2, 64, 8,
                                       128, 2048, 32768, 30720, seed=5)
 
+# Not one of the five workloads: the 8K causal prefill with one query head per KV
+# head (G = 1), for timing the odd-G work items.
+CAUSAL_PREFILL_8K_MHA = PrefillWorkload("mha_causal_prefill_b1_t8192", 1, 64, 64, 128, 8192,
+                                        8192, 0, seed=6)
+
 RAGGED_SEQLEN_SEED = 1003
 RAGGED_SEQLEN_RANGE = (16384, 131072)  # inclusive
 

@@ -37,7 +37,7 @@ def _rank_main(rank, world, port, out):
 
 def test_aggregate_max_over_two_gloo_ranks():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         assert out[0] == out[1] == [1.0, 10.0, 3.0]

@@ -64,9 +64,10 @@ def test_issued_tiles_equal_the_lower_triangle_full_size(DL, w):
 
 
 @pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,off,causal", [
-    (1, 24, 8, 1100, 1300, 200, True),    # G = 3: one head per CTA
+    (1, 24, 8, 1100, 1300, 200, True),    # G = 3: block pairs of different extents
     (2, 16, 2, 300, 300, 0, True),        # ragged last block and tile
     (1, 8, 8, 257, 1000, 743, True),      # G = 1, chunk at the end of the prefix
+    (1, 5, 5, 300, 300, 0, True),         # G = 1, three blocks: the last pair's second is empty
     (1, 16, 2, 200, 333, 0, False),       # full attention: every tile, no class split
 ])
 def test_issued_tiles_and_outputs_small(DL, B, H_q, H_kv, T_q, S_kv, off, causal):

@@ -60,6 +60,11 @@ def run_prefill(q, k, v, q_offset, causal, scale=None):
     (3, 8, 1, 129, 129, 0, True),       # three batch rows, one query row past a block
     (1, 8, 2, 1, 1000, 999, True),      # one query at the end of a long prefix (causal)
     (2, 8, 2, 1, 777, 0, False),        # one query, full attention over ragged keys
+    # odd G: work items pair two consecutive query blocks of one head
+    (1, 5, 5, 129, 700, 571, True),     # G = 1, the second block holds one row
+    (2, 6, 2, 300, 300, 0, False),      # G = 3, full attention; last pair's second block empty
+    (1, 9, 3, 640, 640, 0, True),       # G = 3, five blocks
+    (1, 7, 7, 1, 50, 49, True),         # G = 1, a single query
 ])
 def test_small_shapes(B, H_q, H_kv, T_q, S_kv, off, causal):
     q, k, v = wl.small_prefill(B, H_q, H_kv, 128, T_q, S_kv, off, seed=10 + T_q + S_kv)
@@ -100,7 +105,9 @@ def test_full_size_workloads_every_row(w):
     (2, 64, 8, 1024, 4096, 3072, True),    # chunk at an offset, two batch rows: 512 items
     (1, 64, 8, 1024, 1536, 0, False),      # full attention: 256 items
     (1, 48, 8, 1536, 1536, 0, True),       # G = 6: pairs cross no KV group, 288 items
-    (1, 24, 8, 1100, 1300, 200, True),     # G = 3 (one head per CTA), ragged last block
+    (1, 24, 8, 1100, 1300, 200, True),     # G = 3: block pairs, ragged last block
+    (1, 64, 64, 1024, 1024, 0, True),      # G = 1: 256 block-pair items
+    (2, 48, 16, 700, 1500, 800, True),     # G = 3, two batch rows, chunk at an offset
 ])
 def test_many_work_items_per_cta_every_row(B, H_q, H_kv, T_q, S_kv, off, causal):
     # The persistent kernel runs several items per CTA here: barrier phases

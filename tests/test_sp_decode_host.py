@@ -71,7 +71,7 @@ def _rank(rank, world, port, out):
 
 def test_two_ranks_merge_to_the_whole_row():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
         O, L = np.array(out["o"]), np.array(out["lse"])
