@@ -26,8 +26,11 @@ DEBUG_LIB = os.path.join(PKG, "libgqa_attn_debug.so")
 
 SOURCES = ["plan.cpp", "runtime.cu", "decode.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
-         "--expt-relaxed-constexpr"]
+# Hidden visibility: only the C ABI (GQA_API in include/gqa_attn.h) is exported,
+# so two builds loaded in one process (the product and the -DGQA_DEBUG library)
+# share no C++ symbols, template statics included.
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
+         "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
 
 
 def _nvcc() -> str:

@@ -1889,7 +1889,7 @@ extern "C" int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes,
 }
 
 #ifdef GQA_TRACE
-extern "C" int gqa_attn_trace_dump(void* host, size_t bytes, int clear) {
+extern "C" GQA_API int gqa_attn_trace_dump(void* host, size_t bytes, int clear) {
     if (bytes > sizeof(gqa::g_trace)) bytes = sizeof(gqa::g_trace);
     if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
     if (cudaMemcpyFromSymbol(host, gqa::g_trace, bytes) != cudaSuccess) return GQA_ERR_CUDA;

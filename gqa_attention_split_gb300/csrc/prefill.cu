@@ -34,15 +34,13 @@ namespace prefill {
 
 constexpr int BM = kPrefillBlockM;  // 128 query rows per work item
 constexpr int BN = kPrefillBlockN;  // 128 keys per KV tile
-constexpr int D = 128;
-constexpr uint32_t kBoxBytes = 128 * 128;        // [128 rows][64 bf16]
-constexpr uint32_t kTileBytes = 2 * kBoxBytes;   // [128 rows][128 bf16], two boxes
+constexpr uint32_t kBoxBytes = 128 * 128;        // [128 rows][64 bf16]: one TMA box
 constexpr uint32_t kTmemCols = 512;  // S_0, S_1, O_0, O_1: 128 columns each
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: rescale O when max grows by > 256x
 
 struct Params {
-    uint16_t* o;        // [B, H_q, T_q, D]
+    uint16_t* o;        // [B, H_q, T_q, d]
     float* lse;         // [B, H_q, T_q] or null
     unsigned* status;
     int B, H_q, H_kv, G, T_q, S_kv, q_offset, causal, n_mblocks;
@@ -136,20 +134,29 @@ __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint
 // barrier has parity k & 1 (per group for the S, P and O barriers).
 
 constexpr int kPairThreads = 384;
-// Four 32 KB slots: ring item r (K_j or V_j of some work item) reuses the
-// slot of item r - 4; the loads land well before their MMAs.
+// Four slots of one tile each: ring item r (K_j or V_j of some work item)
+// reuses the slot of item r - 4; the loads land well before their MMAs.
 constexpr int kRingSlots = 4;
-constexpr uint32_t kPairQOff = 0;                                // Q_A, then Q_B
-constexpr uint32_t kPairRingOff = 2 * kTileBytes;                // kRingSlots x 32 KB
 // O leaves through TMA stores: each softmax warp owns two 2 KB buffers, each
 // one [32 rows][32 bf16] box in the 64-byte swizzle (16-byte chunk k of row
 // r at r * 64 + ((k ^ ((r >> 1) & 3)) << 4), so a warp's row-per-lane writes
 // hit distinct banks).
-constexpr uint32_t kPairStageOff = kPairRingOff + kRingSlots * kTileBytes;
 constexpr uint32_t kStageBoxBytes = 32 * 32 * 2;
-constexpr uint32_t kPairBarOff = kPairStageOff + 8 * 2 * kStageBoxBytes;
-constexpr int kPairSmemBytes = 1024 + kPairBarOff + 256;
-static_assert(kPairSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
+
+// Shared-memory layout for head dim D (64 or 128): a tile of 128 rows is D/64
+// boxes of 64 columns.
+template <int D>
+struct PairGeo {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kBoxes = D / 64;
+    static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+    static constexpr uint32_t kQOff = 0;                                  // Q_A, then Q_B
+    static constexpr uint32_t kRingOff = 2 * kTileBytes;                  // kRingSlots tiles
+    static constexpr uint32_t kStageOff = kRingOff + kRingSlots * kTileBytes;
+    static constexpr uint32_t kBarOff = kStageOff + 8 * 2 * kStageBoxBytes;
+    static constexpr int kSmemBytes = 1024 + kBarOff + 256;
+    static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may have");
+};
 // S_g (and P_g over its first 64 columns) at g*128; O_g at 256 + g*128.
 __device__ __forceinline__ uint32_t col_s_of(int g) { return uint32_t(g) * 128u; }
 __device__ __forceinline__ uint32_t col_o_of(int g) { return 256u + uint32_t(g) * 128u; }
@@ -232,17 +239,19 @@ __device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) 
     return true;
 }
 
-template <bool kBlocks>
+template <bool kBlocks, int D>
 __global__ void __launch_bounds__(kPairThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ CUtensorMap tmap_o, const Params p) {
+    using Gm = PairGeo<D>;
+    constexpr uint32_t kTileBytes = Gm::kTileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairBarOff);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPairBarOff + pNumBars * 8);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kBarOff + pNumBars * 8);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -292,8 +301,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 // (an empty group's rows lie past T_q: the copy reads zero fill)
                 mbar_arrive_expect_tx(bar(pQFull), 2 * kTileBytes);
                 for (int g = 0; g < 2; ++g)
-                    for (int hh = 0; hh < 2; ++hh)
-                        tma_load(smem_u32(smem + kPairQOff + g * kTileBytes) + hh * kBoxBytes,
+                    for (int hh = 0; hh < Gm::kBoxes; ++hh)
+                        tma_load(smem_u32(smem + Gm::kQOff + g * kTileBytes) + hh * kBoxBytes,
                                  &tmap_q, hh * 64, kBlocks ? w.row0[g] : w.row0[0],
                                  w.b * p.H_q + (kBlocks ? w.head[g] : w.head[0] + g),
                                  bar(pQFull));
@@ -306,9 +315,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                               p.status);
                 if (!alive) break;
                 const CUtensorMap* map = (i & 1) ? &tmap_v : &tmap_k;
-                const uint32_t dst = smem_u32(smem + kPairRingOff + s * kTileBytes);
+                const uint32_t dst = smem_u32(smem + Gm::kRingOff + s * kTileBytes);
                 mbar_arrive_expect_tx(bar(pSlotFull + s), kTileBytes);
-                for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < Gm::kBoxes; ++hh)
                     tma_load(dst + hh * kBoxBytes, map, hh * 64, (i >> 1) * BN,
                              w.b * p.H_kv + w.kvh, bar(pSlotFull + s));
             }
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false);
         const uint32_t idesc_pv = tc::idesc_bf16_f32(BM, D, true);
         auto slot_addr = [&](int i) {
-            return smem_u32(smem + kPairRingOff + (i % kRingSlots) * kTileBytes);
+            return smem_u32(smem + Gm::kRingOff + (i % kRingSlots) * kTileBytes);
         };
         auto wait_item = [&](int i) {
             return mbar_wait_bounded(bar(pSlotFull + i % kRingSlots), (i / kRingSlots) & 1, p.status);
@@ -333,8 +342,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // Descriptors are built once per operand; each k-step adds its byte
         // offset >> 4 to the 14-bit start-address field (shared addresses
         // stay below 256 KB, so the field never carries out).
-        const uint64_t qdesc0 = tc::sdesc_sw128(smem_u32(smem + kPairQOff), 16, 1024);
-        const uint64_t qdesc1 = tc::sdesc_sw128(smem_u32(smem + kPairQOff + kTileBytes), 16, 1024);
+        const uint64_t qdesc0 = tc::sdesc_sw128(smem_u32(smem + Gm::kQOff), 16, 1024);
+        const uint64_t qdesc1 = tc::sdesc_sw128(smem_u32(smem + Gm::kQOff + kTileBytes), 16, 1024);
         auto issue_s = [&](int g, int ri) {  // S_g = Q_g K^T, K in ring item ri
             const uint64_t qdesc = g ? qdesc1 : qdesc0;
             const uint64_t kdesc = tc::sdesc_sw128(slot_addr(ri), 16, 1024);
@@ -465,7 +474,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
         const uint32_t col_s = col_s_of(g), col_o = col_o_of(g);
-        const uint32_t stage = smem_u32(smem + kPairStageOff + (g * 4 + quad) * 2 * kStageBoxBytes);
+        const uint32_t stage = smem_u32(smem + Gm::kStageOff + (g * 4 + quad) * 2 * kStageBoxBytes);
         const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
         bool alive = true;
         int tt = 0;   // KV tiles this group finished so far, over all work items
@@ -657,13 +666,32 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
     // scale it, which is the maximum of the scaled scores only for scale > 0
     if (H_q % H_kv != 0 || !isfinite(scale) || !(scale > 0.f)) return GQA_ERR_INVALID_ARG;
     if (causal && int64_t(q_offset) + T_q > S_kv) return GQA_ERR_INVALID_ARG;
-    if (d != D) return GQA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
     if (int64_t(B) * H_q * T_q >= (int64_t(1) << 31) ||
         int64_t(B) * H_kv * S_kv >= (int64_t(1) << 31))
         return GQA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return GQA_ERR_MISALIGNED;
     return GQA_OK;
+}
+
+// One launch of the pair kernel for head dim D; function attributes once per
+// device.
+template <bool kBlocks, int D>
+int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                const CUtensorMap& to, const Params& prm, int ctas, cudaStream_t stream) {
+    auto kern = prefill_pair_kernel<kBlocks, D>;
+    static std::atomic<uint64_t> attr_done{0};
+    const int dev = current_device();
+    if (device_attrs_pending(attr_done, dev)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairGeo<D>::kSmemBytes) != cudaSuccess)
+            return GQA_ERR_CUDA;
+        device_attrs_mark(attr_done, dev);
+    }
+    kern<<<dim3(unsigned(ctas)), kPairThreads, PairGeo<D>::kSmemBytes, stream>>>(tq, tk, tv, to,
+                                                                                prm);
+    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 }  // namespace prefill
@@ -682,11 +710,11 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
     CUtensorMap tq, tk, tv, to;
-    if (encode_tmap_3d_bf16(&tq, q, D, T_q, uint64_t(B) * H_q, 64, BM,
+    if (encode_tmap_3d_bf16(&tq, q, d, T_q, uint64_t(B) * H_q, 64, BM,
                             CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
-        encode_tmap_3d_bf16(&tk, k, D, S_kv, uint64_t(B) * H_kv, 64, BN,
+        encode_tmap_3d_bf16(&tk, k, d, S_kv, uint64_t(B) * H_kv, 64, BN,
                             CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
-        encode_tmap_3d_bf16(&tv, v, D, S_kv, uint64_t(B) * H_kv, 64, BN,
+        encode_tmap_3d_bf16(&tv, v, d, S_kv, uint64_t(B) * H_kv, 64, BN,
                             CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
         return GQA_ERR_CUDA;
     Params prm{};
@@ -707,18 +735,6 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     // Even group sizes pair two heads of a KV group per work item; odd ones pair
     // two consecutive query blocks of one head.
     const bool blocks = prm.G % 2 != 0;
-    static std::atomic<uint64_t> attr_done{0};  // once per device
-    const int dev = current_device();
-    if (device_attrs_pending(attr_done, dev)) {
-        if (cudaFuncSetAttribute(prefill_pair_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_pair_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) != cudaSuccess)
-            return GQA_ERR_CUDA;
-        device_attrs_mark(attr_done, dev);
-    }
     const int64_t items = blocks ? int64_t((prm.n_mblocks + 1) / 2) * B * H_q
                                  : int64_t(prm.n_mblocks) * B * (H_q / 2);
     if (items > 0x7fffffff) return GQA_ERR_UNSUPPORTED;
@@ -726,17 +742,14 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     const int sms = num_sms();
     if (sms <= 0) return GQA_ERR_CUDA;
     const int ctas = int(items < int64_t(sms) ? items : int64_t(sms));
-    if (encode_tmap_3d_bf16(&to, o, D, T_q, uint64_t(B) * H_q, 32, 32,
+    if (encode_tmap_3d_bf16(&to, o, d, T_q, uint64_t(B) * H_q, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess)
         return GQA_ERR_CUDA;
-    if (blocks)
-        prefill_pair_kernel<true><<<dim3(unsigned(ctas)), kPairThreads, kPairSmemBytes, stream>>>(
-            tq, tk, tv, to, prm);
-    else
-        prefill_pair_kernel<false><<<dim3(unsigned(ctas)), kPairThreads, kPairSmemBytes,
-                                     stream>>>(tq, tk, tv, to, prm);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    return GQA_OK;
+    if (d == 128)
+        return blocks ? launch_pair<true, 128>(tq, tk, tv, to, prm, ctas, stream)
+                      : launch_pair<false, 128>(tq, tk, tv, to, prm, ctas, stream);
+    return blocks ? launch_pair<true, 64>(tq, tk, tv, to, prm, ctas, stream)
+                  : launch_pair<false, 64>(tq, tk, tv, to, prm, ctas, stream);
 }
 
 extern "C" int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -768,7 +781,7 @@ extern "C" int gqa_attn_debug_tile_counts(int64_t* counts, int clear) {
 }
 
 #ifdef GQA_TRACE
-extern "C" int gqa_attn_trace_dump_prefill(void* host, size_t bytes, int clear) {
+extern "C" GQA_API int gqa_attn_trace_dump_prefill(void* host, size_t bytes, int clear) {
     if (bytes > sizeof(gqa::g_trace)) bytes = sizeof(gqa::g_trace);
     if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
     if (cudaMemcpyFromSymbol(host, gqa::g_trace, bytes) != cudaSuccess) return GQA_ERR_CUDA;

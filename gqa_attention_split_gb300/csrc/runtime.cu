@@ -180,7 +180,7 @@ extern "C" const char* gqa_attn_strerror(int code) {
     switch (code) {
         case GQA_OK: return "ok";
         case GQA_ERR_INVALID_ARG: return "invalid argument";
-        case GQA_ERR_UNSUPPORTED: return "unsupported shape (decode: d 64 or 128 and G <= 16; prefill: d 128)";
+        case GQA_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128; decode: G <= 16)";
         case GQA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
         case GQA_ERR_CUDA: return "CUDA runtime or driver error";
         case GQA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";

@@ -43,6 +43,14 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* The library is built with hidden symbol visibility; only the calls below
+ * are exported. */
+#if defined(__GNUC__)
+#define GQA_API __attribute__((visibility("default")))
+#else
+#define GQA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -53,7 +61,7 @@ typedef struct CUstream_st* cudaStream_t;
 enum {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = -1,    /* null pointer, bad size, H_q % H_kv != 0, ... */
-    GQA_ERR_UNSUPPORTED = -2,    /* decode: d not in {64, 128} or G > 16; prefill: d != 128 */
+    GQA_ERR_UNSUPPORTED = -2,    /* d not in {64, 128}; decode: G > 16 */
     GQA_ERR_MISALIGNED = -3,     /* a tensor pointer is not 16-byte aligned */
     GQA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
     GQA_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (device status) */
@@ -95,25 +103,25 @@ enum {
  * as a CUDA graph, stays valid; the kept buffers together are smaller than the
  * current one. Calls on different streams never share a workspace.
  */
-int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                    uint16_t* o, float* lse, const int32_t* seqlens,
-                    int B, int H_q, int H_kv, int d, int S_max,
-                    float scale, int num_splits, cudaStream_t stream);
+GQA_API int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            uint16_t* o, float* lse, const int32_t* seqlens,
+                            int B, int H_q, int H_kv, int d, int S_max,
+                            float scale, int num_splits, cudaStream_t stream);
 
 /* The same, with a caller-provided device workspace (256-byte aligned) of at
  * least gqa_attn_decode_workspace_size(B, H_q, d, num_splits) bytes; here
  * num_splits must be >= 1 (resolve 0 with gqa_attn_pick_num_splits first).
  * The workspace holds no state between calls; calls that overlap on the GPU
  * must not share one. */
-int gqa_attn_decode_ws(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                       uint16_t* o, float* lse, const int32_t* seqlens,
-                       int B, int H_q, int H_kv, int d, int S_max,
-                       float scale, int num_splits,
-                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+GQA_API int gqa_attn_decode_ws(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               uint16_t* o, float* lse, const int32_t* seqlens,
+                               int B, int H_q, int H_kv, int d, int S_max,
+                               float scale, int num_splits,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of decode workspace for these sizes (0 when num_splits == 1, which
  * writes O directly). Returns 0 on invalid sizes as well. */
-size_t gqa_attn_decode_workspace_size(int B, int H_q, int d, int num_splits);
+GQA_API size_t gqa_attn_decode_workspace_size(int B, int H_q, int d, int num_splits);
 
 /* gqa_attn_decode for callers that must not allocate device memory. (The page
  * has no counterpart: this is a deployment option, not part of the method.)
@@ -140,10 +148,10 @@ size_t gqa_attn_decode_workspace_size(int B, int H_q, int d, int num_splits);
  *     with gqa_attn_check(), which allocates nothing either.
  */
 #define GQA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
-int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                            uint16_t* o, float* lse, const int32_t* seqlens,
-                            int B, int H_q, int H_kv, int d, int S_max,
-                            float scale, int num_splits, cudaStream_t stream);
+GQA_API int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    uint16_t* o, float* lse, const int32_t* seqlens,
+                                    int B, int H_q, int H_kv, int d, int S_max,
+                                    float scale, int num_splits, cudaStream_t stream);
 
 /* ------------------------------------------ sequence-parallel decode ------
  * Page: ADR-0060 §5.3 (decode with sequence parallelism: every rank sweeps its
@@ -162,10 +170,10 @@ int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t
  * and seqlens the rows' key counts inside it.
  *   o_part   : fp32 [B, H_q, d], 16-byte aligned; a row with no keys gets 0.
  *   lse_part : fp32 [B, H_q] (required); a row with no keys gets -inf. */
-int gqa_attn_decode_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                            float* o_part, float* lse_part, const int32_t* seqlens,
-                            int B, int H_q, int H_kv, int d, int S_max, float scale,
-                            int num_splits, cudaStream_t stream);
+GQA_API int gqa_attn_decode_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    float* o_part, float* lse_part, const int32_t* seqlens,
+                                    int B, int H_q, int H_kv, int d, int S_max, float scale,
+                                    int num_splits, cudaStream_t stream);
 
 /* Merges R partials in rank order with the log-sum-exp rule:
  *   lse = ln sum_r exp(lse_r),  O = sum_r exp(lse_r - lse) O_r  (then bf16).
@@ -175,8 +183,8 @@ int gqa_attn_decode_partial(const uint16_t* q, const uint16_t* k, const uint16_t
  *   o         : bf16 [rows, d]; lse: fp32 [rows] or NULL.
  * A row whose parts are all empty gets O = 0 and lse = -inf. d in {64, 128},
  * R >= 1. Async on `stream`; deterministic (fixed order). */
-int gqa_attn_merge(const float* o_parts, const float* lse_parts, uint16_t* o, float* lse,
-                   int R, int rows, int d, cudaStream_t stream);
+GQA_API int gqa_attn_merge(const float* o_parts, const float* lse_parts, uint16_t* o, float* lse,
+                           int R, int rows, int d, cudaStream_t stream);
 
 /* ------------------------------------------ ring-buffer cache with sinks --
  * Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §2 item 4 (a KV
@@ -195,9 +203,9 @@ int gqa_attn_merge(const float* o_parts, const float* lse_parts, uint16_t* o, fl
  * the row's length before this append). A negative position writes nothing
  * and sets the status word's bad-length bit (gqa_attn_check reports
  * GQA_ERR_DEVICE_BAD_INPUT). Async on `stream`; d in {64, 128}. */
-int gqa_attn_ring_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
-                         const uint16_t* v_new, const int32_t* positions, int B, int H_kv,
-                         int d, int capacity, int n_sink, cudaStream_t stream);
+GQA_API int gqa_attn_ring_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
+                                 const uint16_t* v_new, const int32_t* positions, int B, int H_kv,
+                                 int d, int capacity, int n_sink, cudaStream_t stream);
 
 /* Decode over such a cache: arguments as gqa_attn_decode with S_max =
  * capacity, except that seqlens (required, device int32 [B]) counts every
@@ -205,10 +213,10 @@ int gqa_attn_ring_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k
  * live slots, min(seqlens[b], capacity) of them, which are exactly the sink
  * and window tokens; a negative length is clamped to 0 and reported. Uses the
  * library-owned workspace like gqa_attn_decode. */
-int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                         uint16_t* o, float* lse, const int32_t* seqlens,
-                         int B, int H_q, int H_kv, int d, int capacity, int n_sink,
-                         float scale, int num_splits, cudaStream_t stream);
+GQA_API int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 uint16_t* o, float* lse, const int32_t* seqlens,
+                                 int B, int H_q, int H_kv, int d, int capacity, int n_sink,
+                                 float scale, int num_splits, cudaStream_t stream);
 
 /* ------------------------------------------------------- INT8 KV cache ----
  * Page: "Gemma 3N E4B on pccx v002 — Execution / Scheduling", §4 item 3
@@ -225,9 +233,9 @@ int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const uint16_t* v
 
 /* Quantises a bf16 cache k, v [B, H_kv, S, d] into the layouts above.
  * Async on `stream`. */
-int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
-                            uint8_t* v_codes, float* k_scales, float* v_scales, int B, int H_kv,
-                            int S, int d, cudaStream_t stream);
+GQA_API int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
+                                    uint8_t* v_codes, float* k_scales, float* v_scales,
+                                    int B, int H_kv, int S, int d, cudaStream_t stream);
 
 /* Split-KV decode over an INT8 cache: arguments, outputs, split plan,
  * workspace and errors as gqa_attn_decode (num_splits == 0 resolved with
@@ -239,10 +247,11 @@ int gqa_attn_quantize_kv_q8(const uint16_t* k, const uint16_t* v, uint8_t* k_cod
  * softmax weight. Rows, ragged lengths and seqlens behave as in
  * gqa_attn_decode; scales and codes beyond a row's length are never used (they
  * may hold anything). */
-int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes, const uint8_t* v_codes,
-                       const float* k_scales, const float* v_scales, uint16_t* o, float* lse,
-                       const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max,
-                       float scale, int num_splits, cudaStream_t stream);
+GQA_API int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes,
+                               const uint8_t* v_codes, const float* k_scales,
+                               const float* v_scales, uint16_t* o, float* lse,
+                               const int32_t* seqlens, int B, int H_q, int H_kv, int d,
+                               int S_max, float scale, int num_splits, cudaStream_t stream);
 
 /* ------------------------------------------------------- INT4 KV cache ----
  * The same page and recommendation (§4 item 3), with 4-bit codes: one fp32
@@ -258,9 +267,9 @@ int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes, const uint8_t*
 
 /* Quantises a bf16 cache k, v [B, H_kv, S, d] into the layouts above.
  * Async on `stream`. */
-int gqa_attn_quantize_kv_q4(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
-                            uint8_t* v_codes, float* k_scales, float* v_scales, int B, int H_kv,
-                            int S, int d, cudaStream_t stream);
+GQA_API int gqa_attn_quantize_kv_q4(const uint16_t* k, const uint16_t* v, uint8_t* k_codes,
+                                    uint8_t* v_codes, float* k_scales, float* v_scales,
+                                    int B, int H_kv, int S, int d, cudaStream_t stream);
 
 /* Split-KV decode over an INT4 cache: as gqa_attn_decode_q8 (num_splits == 0
  * resolved with gqa_attn_pick_num_splits_q4). The result is attention over
@@ -270,10 +279,11 @@ int gqa_attn_quantize_kv_q4(const uint16_t* k, const uint16_t* v, uint8_t* k_cod
  * values by 1/16, takes the offsets off once per head, and applies the K
  * scale to each token's scores and the V scale to each token's softmax
  * weight. */
-int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes, const uint8_t* v_codes,
-                       const float* k_scales, const float* v_scales, uint16_t* o, float* lse,
-                       const int32_t* seqlens, int B, int H_q, int H_kv, int d, int S_max,
-                       float scale, int num_splits, cudaStream_t stream);
+GQA_API int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes,
+                               const uint8_t* v_codes, const float* k_scales,
+                               const float* v_scales, uint16_t* o, float* lse,
+                               const int32_t* seqlens, int B, int H_q, int H_kv, int d,
+                               int S_max, float scale, int num_splits, cudaStream_t stream);
 
 /* --------------------------------------------------------------- prefill --
  * gqa_attn_prefill: T_q new queries at global positions q_offset + t against
@@ -282,20 +292,20 @@ int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes, const uint8_t*
  * future KV tiles are skipped and partial tiles masked (§5.4). causal == 0:
  * every key is visible. Fixed to the Llama3-70B head geometry of §0
  * (H_q = 64, H_kv = 8, d = 128); gqa_attn_prefill_ex takes any supported one
- * (d = 128, any H_q divisible by H_kv).
+ * (d = 64 or 128, any H_q divisible by H_kv).
  *   lse   : [B, H_q, T_q] fp32, or NULL.
  *   scale : softmax scale, finite and > 0 (§0.5 fixes 1/sqrt(d)); anything
  *           else returns GQA_ERR_INVALID_ARG.
  */
-int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                     uint16_t* o, float* lse,
-                     int B, int T_q, int S_kv, int q_offset, int causal,
-                     float scale, cudaStream_t stream);
+GQA_API int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             uint16_t* o, float* lse,
+                             int B, int T_q, int S_kv, int q_offset, int causal,
+                             float scale, cudaStream_t stream);
 
-int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                        uint16_t* o, float* lse,
-                        int B, int H_q, int H_kv, int d, int T_q, int S_kv,
-                        int q_offset, int causal, float scale, cudaStream_t stream);
+GQA_API int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                uint16_t* o, float* lse,
+                                int B, int H_q, int H_kv, int d, int T_q, int S_kv,
+                                int q_offset, int causal, float scale, cudaStream_t stream);
 
 /* ------------------------------------------------------ plan / scheduler --
  * Integer helpers the kernels use, exported so tests can compare them with
@@ -308,20 +318,20 @@ int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * ceil(S_max / 1024) (rounded up to a multiple of 16 when above 16), and at
  * most max(1, S_max / 256) so no split is shorter than 256 keys. Returns
  * >= 1, or GQA_ERR_INVALID_ARG. */
-int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
+GQA_API int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
 
 /* Split count for a decode over an INT8 cache: gqa_attn_pick_num_splits for a
  * row of ceil(S_max / 2) keys. The split-length bounds above are sized in
  * bytes, and an INT8 token (2 x d code bytes + 2 fp32 scales) is about half
  * a bf16 token (4 x d bytes). Returns >= 1, or GQA_ERR_INVALID_ARG. */
-int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_sms);
+GQA_API int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_sms);
 
 /* Split count for a decode over an INT4 cache: the INT8 rule,
  * gqa_attn_pick_num_splits_q8. An INT4 token is about a quarter of a bf16 one
  * in bytes, but both quantised decodes are bound by instruction issue rather
  * than bytes, and measured faster with the INT8 split counts. Returns >= 1, or
  * GQA_ERR_INVALID_ARG. */
-int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms);
+GQA_API int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms);
 
 /* Cluster size a decode launch uses on a GPU with num_sms SMs: the largest of
  * 16, 8, 4, 2 that divides num_splits (else 1), at most 8 when the grid of
@@ -331,26 +341,26 @@ int gqa_attn_pick_num_splits_q4(int B, int H_kv, int S_max, int num_sms);
  * The splits of one cluster are merged on chip; a row spanning several
  * clusters is finished by the combine kernel. Returns the size, or
  * GQA_ERR_INVALID_ARG. */
-int gqa_attn_decode_cluster_size(int B, int H_kv, int num_splits, int num_sms);
+GQA_API int gqa_attn_decode_cluster_size(int B, int H_kv, int num_splits, int num_sms);
 
 /* Fills starts[s], ends[s] (s < num_splits) with the decode split plan above
  * for one row of length seqlen (0 <= seqlen <= S_max). */
-int gqa_attn_split_bounds(int S_max, int num_splits, int seqlen,
-                          int32_t* starts, int32_t* ends);
+GQA_API int gqa_attn_split_bounds(int S_max, int num_splits, int seqlen,
+                                  int32_t* starts, int32_t* ends);
 
 /* §5.4 classification of query block [qs, qe) against KV tile [ks, ke), in
  * global positions: 0 = all past (ke <= qs, no mask), 2 = all future
  * (ks >= qe, skipped), 1 = partial (masked). */
-int gqa_attn_tile_class(int qs, int qe, int ks, int ke);
+GQA_API int gqa_attn_tile_class(int qs, int qe, int ks, int ke);
 
 /* Tile counts of the prefill kernel's own schedule for one (batch, head):
  * query blocks of gqa_attn_prefill_block_m() rows, KV tiles of
  * gqa_attn_prefill_block_n() keys, classified as above. Writes the number of
  * all-past, partial and all-future (skipped) tile pairs. */
-int gqa_attn_prefill_tile_counts(int T_q, int S_kv, int q_offset, int causal,
-                                 int64_t* n_past, int64_t* n_partial, int64_t* n_future);
-int gqa_attn_prefill_block_m(void);
-int gqa_attn_prefill_block_n(void);
+GQA_API int gqa_attn_prefill_tile_counts(int T_q, int S_kv, int q_offset, int causal,
+                                         int64_t* n_past, int64_t* n_partial, int64_t* n_future);
+GQA_API int gqa_attn_prefill_block_m(void);
+GQA_API int gqa_attn_prefill_block_n(void);
 
 /* ------------------------------------------------------------ status ----- */
 
@@ -358,7 +368,7 @@ int gqa_attn_prefill_block_n(void);
  * current device (allocates no memory). Returns GQA_OK,
  * GQA_ERR_DEVICE_TIMEOUT, GQA_ERR_DEVICE_BAD_INPUT or GQA_ERR_CUDA. The word
  * collects the errors of every call on that device since the last check. */
-int gqa_attn_check(cudaStream_t stream);
+GQA_API int gqa_attn_check(cudaStream_t stream);
 
 /* Test hook for failure reporting: the next `launches` decode or prefill
  * calls (gqa_attn_decode*, gqa_attn_prefill*) each make their first block
@@ -368,7 +378,7 @@ int gqa_attn_check(cudaStream_t stream);
  * normally, and gqa_attn_check() returns GQA_ERR_DEVICE_TIMEOUT. The output of
  * such a call is undefined; nothing faults and later calls are unaffected.
  * 0 disarms. Returns GQA_OK or GQA_ERR_INVALID_ARG (launches < 0). */
-int gqa_attn_debug_inject_timeout(int launches);
+GQA_API int gqa_attn_debug_inject_timeout(int launches);
 
 /* Causal-skip check (page: ADR-0060 §11, verification plan: the number of
  * tile GEMMs equals the lower-triangle tile count). In a library built with
@@ -379,13 +389,13 @@ int gqa_attn_debug_inject_timeout(int launches);
  * all-future tiles issued since the last clear, and zeroes the counters when
  * clear != 0. A correct schedule issues no all-future tile. Other builds
  * return GQA_ERR_UNSUPPORTED and touch nothing. */
-int gqa_attn_debug_tile_counts(int64_t* counts, int clear);
+GQA_API int gqa_attn_debug_tile_counts(int64_t* counts, int clear);
 
 /* Static, human-readable text for a return code. */
-const char* gqa_attn_strerror(int code);
+GQA_API const char* gqa_attn_strerror(int code);
 
 /* Library version as major * 10000 + minor * 100 + patch. */
-int gqa_attn_version(void);
+GQA_API int gqa_attn_version(void);
 
 #ifdef __cplusplus
 }

@@ -199,8 +199,8 @@ def test_decode_empty_batch_is_a_no_op(L):
      api.GQA_ERR_INVALID_ARG),
     ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 128, 128, 128, 0, 1, float("nan")),
      api.GQA_ERR_INVALID_ARG),
-    # prefill runs d = 128 only
-    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 64, 128, 128, 0, 1, 0.1), api.GQA_ERR_UNSUPPORTED),
+    # prefill runs d = 64 and 128
+    ((FAKE, FAKE, FAKE, FAKE, 0, 1, 64, 8, 96, 128, 128, 0, 1, 0.1), api.GQA_ERR_UNSUPPORTED),
 ])
 def test_prefill_bad_args_return_codes_without_launch(L, args, code):
     assert api.gqa_attn_prefill_ex(*args, None) == code
@@ -289,3 +289,23 @@ def test_q4_bad_args_return_codes_without_launch(L):
                                   0.1, 0, st) == api.GQA_ERR_UNSUPPORTED
     assert api.gqa_attn_decode_q4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, 8, 1, 128, 64,
                                   0.1, 0, st) == 0                       # empty batch
+
+
+def test_only_the_c_abi_is_exported(L):
+    # The library is built with hidden visibility: its C++ internals (launch
+    # helpers, their per-device "attributes set" statics, template kernels)
+    # are private to each build, so the product library and the -DGQA_DEBUG
+    # build can live in one process. Process-unique symbols would be merged
+    # across the two by the dynamic linker.
+    import shutil
+    import subprocess
+
+    if shutil.which("nm") is None:
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--defined-only", api.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = [ln.split() for ln in out.splitlines() if len(ln.split()) == 3]
+    assert not [s for s in syms if s[1] == "u"], "process-unique symbols exported"
+    ours = sorted(s[2] for s in syms if s[2].startswith("gqa_attn_"))
+    assert ours == sorted(api.symbols())
+    assert not [s for s in syms if "gqa" in s[2] and not s[2].startswith("gqa_attn_")]

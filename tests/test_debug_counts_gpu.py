@@ -70,14 +70,15 @@ def test_issued_tiles_equal_the_lower_triangle_full_size(DL, w):
     (1, 5, 5, 300, 300, 0, True),         # G = 1, three blocks: the last pair's second is empty
     (1, 16, 2, 200, 333, 0, False),       # full attention: every tile, no class split
 ])
-def test_issued_tiles_and_outputs_small(DL, B, H_q, H_kv, T_q, S_kv, off, causal):
-    q, k, v = wl.small_prefill(B, H_q, H_kv, 128, T_q, S_kv, off, seed=40 + T_q)
+@pytest.mark.parametrize("d", [64, 128])
+def test_issued_tiles_and_outputs_small(DL, B, H_q, H_kv, T_q, S_kv, off, causal, d):
+    q, k, v = wl.small_prefill(B, H_q, H_kv, d, T_q, S_kv, off, seed=40 + T_q)
     assert api.gqa_attn_debug_tile_counts(clear=True, L=DL)[0] == api.GQA_OK
     o, lse = _prefill(DL, q.cuda(), k.cuda(), v.cuda(), off, causal)
     rc, got = api.gqa_attn_debug_tile_counts(clear=True, L=DL)
     assert rc == api.GQA_OK
     assert got == _expected(B, H_q, T_q, S_kv, off, causal)
-    O, L = orc.attention(q, k, v, scale=1 / math.sqrt(128), causal=causal, q_offset=off)
+    O, L = orc.attention(q, k, v, scale=1 / math.sqrt(d), causal=causal, q_offset=off)
     err = np.abs(o.float().cpu().double().numpy() - O)
     assert err.max() <= 1e-2 and err.mean() <= 1e-3
     assert np.abs(lse.cpu().double().numpy() - L).max() <= 1e-3

@@ -140,6 +140,22 @@ def p_rounding_bound(q, k, v, O, *, causal, q_offset):
     return 2.0 ** -7 * spread + 2.0 ** -8 * np.abs(O) + 1e-4
 
 
+@pytest.mark.parametrize("B,H_q,H_kv,T_q,S_kv,off,causal", [
+    (1, 8, 2, 300, 300, 0, True),         # head pairs, ragged last block and tile
+    (2, 16, 2, 200, 333, 0, False),       # full attention, ragged keys
+    (1, 8, 2, 130, 400, 270, True),       # chunk at an offset
+    (1, 6, 2, 257, 300, 43, True),        # odd G = 3: block pairs
+    (1, 64, 8, 1024, 1024, 0, True),      # 256 items over at most 152 CTAs
+    (1, 32, 32, 640, 640, 0, True),       # G = 1, five blocks
+])
+def test_head_dim_64(B, H_q, H_kv, T_q, S_kv, off, causal):
+    # d = 64: one 64-column box per tile, four k-steps per S MMA, N = 64 for P.V
+    q, k, v = wl.small_prefill(B, H_q, H_kv, 64, T_q, S_kv, off, seed=90 + T_q + H_q)
+    o, lse = run_prefill(q, k, v, off, causal)
+    O, L = attention_by_group(q, k, v, scale=1 / math.sqrt(64), causal=causal, q_offset=off)
+    assert_close(o, lse, O, L, f"d=64 B={B} H={H_q}/{H_kv} T={T_q} S={S_kv} off={off}")
+
+
 @pytest.mark.parametrize("scale", [0.05, 0.3])
 @pytest.mark.parametrize("causal", [True, False])
 def test_scales_other_than_one_over_sqrt_d(scale, causal):
