@@ -91,9 +91,13 @@ def prefill_bytes(B, H_q, H_kv, d, T_q, S_kv):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock and throttle-reason samples every 10 ms; stop(window)
+    keeps the samples taken inside the timed region (wall-clock seconds)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -106,12 +110,12 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "20"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -119,14 +123,15 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
+        lines = open(self.path).read().splitlines()
         os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return self.summarise(lines, window)
+
+    @classmethod
+    def summarise(cls, lines, window=None):
+        """Median SM clock, max clock and active throttle reasons of the samples
+        whose timestamps fall in `window` (t0, t1) (all samples if none do)."""
+        import datetime
 
         def num(x):
             try:
@@ -134,13 +139,30 @@ class ClockSampler:
             except ValueError:
                 return None
 
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        def stamp(x):
+            try:
+                return datetime.datetime.strptime(x, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+
+        rows = [[x.strip() for x in ln.split(",")] for ln in lines]
+        rows = [r for r in rows if len(r) >= 10]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_total": 0}
+        inside = rows
+        if window is not None:
+            t0, t1 = window
+            inside = [r for r in rows
+                      if stamp(r[0]) is not None and t0 - 0.005 <= stamp(r[0]) <= t1 + 0.005]
+        use = inside or rows
+        sm = [num(r[2]) for r in use if num(r[2]) is not None]
+        mx = [num(r[3]) for r in use if num(r[3]) is not None]
+        reasons = sorted({cls.REASONS[i] for r in use for i in range(4) if r[6 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(inside), "samples_total": len(rows),
+                "window": "timed region" if inside else "whole run (no sample inside it)"}
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -352,13 +374,16 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)  # let the sampler take its first readings
     t_wall0 = time.perf_counter()
+    t_epoch0 = time.time()
     for i in range(args.steps):
         one_step(evs[i])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
+    t_epoch1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    time.sleep(0.05)  # the sampler's last readings of the region
+    clk = clocks.stop(window=(t_epoch0, t_epoch1))
     api.check(stream)
 
     # the same 80 decode calls as plain launches (no graph), after the timed

@@ -110,3 +110,24 @@ def test_decode_bytes_and_prefill_flops_match_closed_forms():
     assert bench.prefill_flops(1, 64, 128, 8192, 8192, 0, True) == 4 * 128 * 64 * 8192 * 8193 // 2
     # chunked: sum_{i<2048} (30721 + i) = 65,012,736 pairs per head and batch row
     assert bench.prefill_flops(2, 64, 128, 2048, 32768, 30720, True) == 4 * 128 * 64 * 2 * 65_012_736
+
+
+def test_clock_samples_are_kept_inside_the_timed_region():
+    rows = ["2026/12/02 10:00:00.000, 0, 1400, 2070, 300.0, 0x0, Not Active, Not Active, "
+            "Not Active, Not Active",
+            "2026/12/02 10:00:01.000, 0, 2070, 2070, 1200.0, 0x4, Not Active, Not Active, "
+            "Not Active, Active",
+            "2026/12/02 10:00:01.010, 0, 2055, 2070, 1250.0, 0x0, Not Active, Not Active, "
+            "Not Active, Not Active",
+            "2026/12/02 10:00:03.000, 0, 900, 2070, 200.0, 0x0, Active, Not Active, "
+            "Not Active, Not Active"]
+    import datetime
+
+    t = lambda s_: datetime.datetime.strptime(s_, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    c = bench.ClockSampler.summarise(rows, (t("2026/12/02 10:00:00.990"),
+                                            t("2026/12/02 10:00:01.020")))
+    assert c["samples"] == 2 and c["samples_total"] == 4
+    assert c["sm_mhz"] == (2070 + 2055) / 2 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]          # not the idle samples' hw_slowdown
+    c = bench.ClockSampler.summarise(rows, (0.0, 1.0))  # nothing inside: all samples
+    assert c["samples"] == 0 and c["samples_total"] == 4 and "hw_slowdown" in c["reasons"]
