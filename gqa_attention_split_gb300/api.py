@@ -47,6 +47,8 @@ _SIGNATURES = {
     "gqa_attn_decode_ring": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "gqa_attn_prefill_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "gqa_attn_prefill_partial": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                      _F, _P]),
     "gqa_attn_pick_num_splits": (_I, [_I, _I, _I, _I]),
     "gqa_attn_pick_num_splits_q8": (_I, [_I, _I, _I, _I]),
     "gqa_attn_pick_num_splits_q4": (_I, [_I, _I, _I, _I]),
@@ -143,6 +145,12 @@ def gqa_attn_prefill_ex(q, k, v, o, lse, B, H_q, H_kv, d, T_q, S_kv, q_offset, c
                         stream):
     return lib().gqa_attn_prefill_ex(q, k, v, o, lse, B, H_q, H_kv, d, T_q, S_kv, q_offset,
                                      causal, scale, stream)
+
+
+def gqa_attn_prefill_partial(q, k, v, o_part, lse_part, B, H_q, H_kv, d, T_q, S_kv, q_offset,
+                             key_offset, causal, scale, stream):
+    return lib().gqa_attn_prefill_partial(q, k, v, o_part, lse_part, B, H_q, H_kv, d, T_q, S_kv,
+                                          q_offset, key_offset, causal, scale, stream)
 
 
 def gqa_attn_pick_num_splits(B, H_kv, S_max, num_sms):
@@ -550,6 +558,33 @@ def prefill(q, k, v, *, q_offset: int = 0, causal: bool = True, scale: float | N
                              T_q, S_kv, q_offset, 1 if causal else 0, sc, _stream_ptr(stream))
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_attn_prefill")
+    return out, lse
+
+
+def prefill_partial(q, k, v, *, q_offset: int = 0, key_offset: int = 0, causal: bool = True,
+                    scale: float | None = None, out=None, lse=None, stream=None):
+    """Prefill against one slice of the keys (global positions key_offset + j),
+    O in fp32 for ``merge``. q [B,H_q,T_q,d], k/v [B,H_kv,S_slice,d] bf16 CUDA.
+    Returns (o fp32 [B,H_q,T_q,d], lse [B,H_q,T_q])."""
+    import torch
+
+    _check_cuda_bf16("q", q, 4)
+    _check_cuda_bf16("k", k, 4)
+    _check_cuda_bf16("v", v, 4)
+    B, H_q, T_q, d = q.shape
+    H_kv, S_kv = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H_kv, S_slice, d] matching q")
+    if out is None:
+        out = torch.empty((B, H_q, T_q, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = gqa_attn_prefill_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv,
+                                  d, T_q, S_kv, q_offset, key_offset, 1 if causal else 0, sc,
+                                  _stream_ptr(stream))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_attn_prefill_partial")
     return out, lse
 
 

@@ -41,6 +41,7 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units: rescale O when max grow
 
 struct Params {
     uint16_t* o;        // [B, H_q, T_q, d]
+    float* o32;         // partial prefill: O in fp32 instead of o
     float* lse;         // [B, H_q, T_q] or null
     unsigned* status;
     int B, H_q, H_kv, G, T_q, S_kv, q_offset, causal, n_mblocks;
@@ -195,7 +196,9 @@ struct PairItem {
 
 // kBlocks: the groups are two query blocks of one head (odd G), else one
 // block of two heads (even G; then both groups share row0, qs, qe and n).
-template <bool kBlocks>
+// kPartial: a prefill over one slice of the keys, where the query offset
+// relative to the slice may be negative and a block may see no key (n = 0).
+template <bool kBlocks, bool kPartial>
 __device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) {
     const int G = gridDim.x, c = blockIdx.x;
     const int L = it * G + ((it & 1) ? G - 1 - c : c);
@@ -217,7 +220,10 @@ __device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) 
             w.qs[g] = p.q_offset + w.row0[g];
             w.qe[g] = p.q_offset + min(w.row0[g] + BM, p.T_q);
             int n = w.row0[g] < p.T_q ? tiles : 0;
-            if (p.causal && n > 0) n = min(n, (w.qe[g] - 1) / BN + 1);  // all-future tiles skipped
+            if (p.causal && n > 0) {
+                if (kPartial && w.qe[g] <= 0) n = 0;  // the slice starts past these queries
+                else n = min(n, (w.qe[g] - 1) / BN + 1);  // all-future tiles skipped
+            }
             w.n[g] = n;
         }
         w.n_tiles = max(w.n[0], w.n[1]);
@@ -235,11 +241,19 @@ __device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) 
         w.qe[0] = p.q_offset + min(m * BM + BM, p.T_q);
         w.n_tiles = (p.S_kv + BN - 1) / BN;
         if (p.causal) w.n_tiles = min(w.n_tiles, (w.qe[0] - 1) / BN + 1);  // all-future skipped
+        if constexpr (kPartial) {  // the per-group path reads every field
+            if (p.causal && w.qe[0] <= 0) w.n_tiles = 0;
+            w.head[1] = h + 1;
+            w.row0[1] = w.row0[0];
+            w.qs[1] = w.qs[0];
+            w.qe[1] = w.qe[0];
+            w.n[0] = w.n[1] = w.n_tiles;
+        }
     }
     return true;
 }
 
-template <bool kBlocks, int D>
+template <bool kBlocks, int D, bool kPartial = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
@@ -247,6 +261,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_o, const Params p) {
     using Gm = PairGeo<D>;
     constexpr uint32_t kTileBytes = Gm::kTileBytes;
+    // per-group bookkeeping: block pairs, or slices where a group may see no key
+    constexpr bool kGen = kBlocks || kPartial;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -291,7 +307,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         bool alive = true;
         int r = 0;        // ring items issued so far, over all work items
         int q_loads = 0;  // Q loads issued (one per work item)
-        for (int it = 0; alive && pair_item<kBlocks>(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, it, w); ++it) {
             // Q of both heads; the previous item's last S MMAs must be done.
             if (it > 0) alive = mbar_wait_bounded(bar(pQEmpty), (it - 1) & 1, p.status);
             if (!alive) break;
@@ -371,12 +387,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         int r = 0;                // ring items consumed so far
         int tt[2] = {0, 0};       // KV tiles group g finished so far (its S and P phases)
         GQA_DBG(unsigned long long dbg[3] = {0, 0, 0};)
-        for (int it = 0; alive && pair_item<kBlocks>(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, it, w); ++it) {
             const int n = w.n_tiles;
+            if constexpr (kPartial) {
+                if (n == 0) {  // no group sees a key of this slice: Q is free again
+                    alive = mbar_wait_bounded(bar(pQFull), it & 1, p.status);
+                    tc::commit(bar(pQEmpty));
+                    continue;
+                }
+            }
             alive = mbar_wait_bounded(bar(pQFull), it & 1, p.status) && wait_item(r);
             if (!alive) break;
             tc::fence_after_sync();
-            if constexpr (!kBlocks) {
+            if constexpr (!kGen) {
                 // two heads, one query block: both groups run every tile
                 issue_s(0, r);
                 issue_s(1, r);
@@ -479,11 +502,25 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         bool alive = true;
         int tt = 0;   // KV tiles this group finished so far, over all work items
         [[maybe_unused]] int itg = 0;  // block pairs: items in which this group had tiles
-        for (int it = 0; alive && pair_item<kBlocks>(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, it, w); ++it) {
             // this group's fields (selected, not indexed: they stay in registers)
-            const int ng = kBlocks ? (g ? w.n[1] : w.n[0]) : w.n_tiles;
-            if constexpr (kBlocks) {
-                if (ng == 0) continue;  // an empty group (past the last query): no MMAs
+            const int ng = kGen ? (g ? w.n[1] : w.n[0]) : w.n_tiles;
+            if constexpr (kGen) {
+                if (ng == 0) {  // past the last query, or (slices) no key visible: no MMAs
+                    if constexpr (kPartial) {  // these rows' result: O = 0, lse = -inf
+                        const int row0_z = kBlocks && g ? w.row0[1] : w.row0[0];
+                        const int head_z = kBlocks ? w.head[0] : w.head[0] + g;
+                        if (row0_z + row < p.T_q) {
+                            const size_t orow =
+                                (size_t(w.b) * p.H_q + head_z) * p.T_q + row0_z + row;
+                            float4* dst = reinterpret_cast<float4*>(p.o32 + orow * D);
+#pragma unroll
+                            for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            p.lse[orow] = -INFINITY;
+                        }
+                    }
+                    continue;
+                }
             }
             const int qs_g = kBlocks && g ? w.qs[1] : w.qs[0];
             const int qe_g = kBlocks && g ? w.qe[1] : w.qe[0];
@@ -532,7 +569,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 m_run = m_use;
                 // p = 2^(s*scale - m): sums of p and of bf16(p); P (bf16 pairs,
                 // lower key in the low half) over the first 64 columns of S.
-                const uint64_t n2 = f2pack(-m_use, -m_use);
+                // (slices: a row that has seen no visible key keeps m = -inf; its
+                // p must come out 0, not NaN, so it subtracts 0 instead)
+                const float m_sub = (kPartial && m_use == -INFINITY) ? 0.f : m_use;
+                const uint64_t n2 = f2pack(-m_sub, -m_sub);
                 uint64_t s2[4];
                 float bl[4], bh[4];
 #pragma unroll
@@ -603,14 +643,39 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // read of O_g completes (wait::ld) before this warp's next P
             // arrive, which is what lets the next item's PV_g(0) overwrite O_g.
             alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(pODone + g),
-                                                              (kBlocks ? itg : it) & 1, p.status));
+                                                              (kGen ? itg : it) & 1, p.status));
             if (!alive) break;
             tc::fence_after_sync();
             const int row0_g = kBlocks && g ? w.row0[1] : w.row0[0];
             const int head_g = kBlocks ? w.head[0] : w.head[0] + g;
             const bool valid = row0_g + row < p.T_q;
-            const float inv = 1.f / lb_run;
             const size_t orow = (size_t(w.b) * p.H_q + head_g) * p.T_q + row0_g + row;
+            if constexpr (kPartial) {
+                // fp32 O for the merge, row by row; a row that saw no key of the
+                // slice gets O = 0 and lse = -inf
+                const float inv = lb_run > 0.f ? 1.f / lb_run : 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(lane_base + col_o + c * 32, r);
+                    tc::tmem_wait_ld();
+                    if (valid) {
+                        float4* dst = reinterpret_cast<float4*>(p.o32 + orow * D + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv,
+                                                 __uint_as_float(r[4 * i + 1]) * inv,
+                                                 __uint_as_float(r[4 * i + 2]) * inv,
+                                                 __uint_as_float(r[4 * i + 3]) * inv);
+                    }
+                }
+                if (valid)
+                    p.lse[orow] = lb_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+                tt += ng;
+                ++itg;
+                continue;
+            }
+            const float inv = 1.f / lb_run;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -643,7 +708,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
             if (valid && p.lse) p.lse[orow] = (m_run + __log2f(l_run)) * kLn2;
             tt += ng;
-            if constexpr (kBlocks) ++itg;
+            if constexpr (kGen) ++itg;
         }
         // the O stores finish before the CTA (and its shared memory) does
         if (lane == 0) bulk_wait_group_all();
@@ -658,14 +723,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 }
 
 int check_args(const void* q, const void* k, const void* v, const void* o, int B, int H_q,
-               int H_kv, int d, int T_q, int S_kv, int q_offset, int causal, float scale) {
+               int H_kv, int d, int T_q, int S_kv, int q_offset, float scale) {
     if (!q || !k || !v || !o) return GQA_ERR_INVALID_ARG;
     if (B < 0 || B > 65535 || H_q <= 0 || H_kv <= 0 || T_q < 0 || S_kv < 1 || q_offset < 0)
         return GQA_ERR_INVALID_ARG;
     // scale > 0: the kernels take each row's maximum over the raw scores and
     // scale it, which is the maximum of the scaled scores only for scale > 0
     if (H_q % H_kv != 0 || !isfinite(scale) || !(scale > 0.f)) return GQA_ERR_INVALID_ARG;
-    if (causal && int64_t(q_offset) + T_q > S_kv) return GQA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
     if (int64_t(B) * H_q * T_q >= (int64_t(1) << 31) ||
         int64_t(B) * H_kv * S_kv >= (int64_t(1) << 31))
@@ -677,10 +741,10 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
 
 // One launch of the pair kernel for head dim D; function attributes once per
 // device.
-template <bool kBlocks, int D>
+template <bool kBlocks, int D, bool kPartial>
 int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                 const CUtensorMap& to, const Params& prm, int ctas, cudaStream_t stream) {
-    auto kern = prefill_pair_kernel<kBlocks, D>;
+    auto kern = prefill_pair_kernel<kBlocks, D, kPartial>;
     static std::atomic<uint64_t> attr_done{0};
     const int dev = current_device();
     if (device_attrs_pending(attr_done, dev)) {
@@ -694,19 +758,13 @@ int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap&
     return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-}  // namespace prefill
-}  // namespace gqa
-
-using namespace gqa;
-
-extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                   uint16_t* o, float* lse, int B, int H_q, int H_kv, int d,
-                                   int T_q, int S_kv, int q_offset, int causal, float scale,
-                                   cudaStream_t stream) {
-    using namespace gqa::prefill;
-    int rc = check_args(q, k, v, o, B, H_q, H_kv, d, T_q, S_kv, q_offset, causal, scale);
-    if (rc != GQA_OK) return rc;
-    if (B == 0 || T_q == 0) return GQA_OK;
+// Both entry points: queries at global positions q_offset + t against keys
+// at key_offset + j (key_offset = 0 for a whole cache); o32 set: the fp32
+// partial output of one slice.
+int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* o32,
+        float* lse, int B, int H_q, int H_kv, int d, int T_q, int S_kv, int q_offset,
+        int key_offset, int causal, float scale, cudaStream_t stream) {
+    const bool partial = o32 != nullptr;
     unsigned* status = status_word();
     if (!status) return GQA_ERR_CUDA;
     CUtensorMap tq, tk, tv, to;
@@ -719,6 +777,7 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
         return GQA_ERR_CUDA;
     Params prm{};
     prm.o = o;
+    prm.o32 = o32;
     prm.lse = lse;
     prm.status = status;
     prm.B = B;
@@ -727,7 +786,9 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     prm.G = H_q / H_kv;
     prm.T_q = T_q;
     prm.S_kv = S_kv;
-    prm.q_offset = causal ? q_offset : 0;
+    // the kernels see the queries' offset relative to the first key (may be
+    // negative for a slice that starts past some queries)
+    prm.q_offset = causal ? q_offset - key_offset : 0;
     prm.causal = causal ? 1 : 0;
     prm.n_mblocks = (T_q + BM - 1) / BM;
     prm.scale_log2 = scale * 1.4426950408889634f;
@@ -742,14 +803,52 @@ extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const u
     const int sms = num_sms();
     if (sms <= 0) return GQA_ERR_CUDA;
     const int ctas = int(items < int64_t(sms) ? items : int64_t(sms));
+    if (partial) {  // O leaves through plain fp32 stores; the O map is not read
+        to = tq;
+        if (d == 128)
+            return blocks ? launch_pair<true, 128, true>(tq, tk, tv, to, prm, ctas, stream)
+                          : launch_pair<false, 128, true>(tq, tk, tv, to, prm, ctas, stream);
+        return blocks ? launch_pair<true, 64, true>(tq, tk, tv, to, prm, ctas, stream)
+                      : launch_pair<false, 64, true>(tq, tk, tv, to, prm, ctas, stream);
+    }
     if (encode_tmap_3d_bf16(&to, o, d, T_q, uint64_t(B) * H_q, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess)
         return GQA_ERR_CUDA;
     if (d == 128)
-        return blocks ? launch_pair<true, 128>(tq, tk, tv, to, prm, ctas, stream)
-                      : launch_pair<false, 128>(tq, tk, tv, to, prm, ctas, stream);
-    return blocks ? launch_pair<true, 64>(tq, tk, tv, to, prm, ctas, stream)
-                  : launch_pair<false, 64>(tq, tk, tv, to, prm, ctas, stream);
+        return blocks ? launch_pair<true, 128, false>(tq, tk, tv, to, prm, ctas, stream)
+                      : launch_pair<false, 128, false>(tq, tk, tv, to, prm, ctas, stream);
+    return blocks ? launch_pair<true, 64, false>(tq, tk, tv, to, prm, ctas, stream)
+                  : launch_pair<false, 64, false>(tq, tk, tv, to, prm, ctas, stream);
+}
+
+}  // namespace prefill
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   uint16_t* o, float* lse, int B, int H_q, int H_kv, int d,
+                                   int T_q, int S_kv, int q_offset, int causal, float scale,
+                                   cudaStream_t stream) {
+    int rc = prefill::check_args(q, k, v, o, B, H_q, H_kv, d, T_q, S_kv, q_offset, scale);
+    if (rc != GQA_OK) return rc;
+    if (causal && int64_t(q_offset) + T_q > S_kv) return GQA_ERR_INVALID_ARG;
+    if (B == 0 || T_q == 0) return GQA_OK;
+    return prefill::run(q, k, v, o, nullptr, lse, B, H_q, H_kv, d, T_q, S_kv, q_offset, 0,
+                        causal, scale, stream);
+}
+
+extern "C" int gqa_attn_prefill_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                        float* o_part, float* lse_part, int B, int H_q, int H_kv,
+                                        int d, int T_q, int S_kv, int q_offset, int key_offset,
+                                        int causal, float scale, cudaStream_t stream) {
+    if (!lse_part || (reinterpret_cast<uintptr_t>(lse_part) & 3u) || key_offset < 0)
+        return GQA_ERR_INVALID_ARG;
+    int rc = prefill::check_args(q, k, v, o_part, B, H_q, H_kv, d, T_q, S_kv, q_offset, scale);
+    if (rc != GQA_OK) return rc;
+    if (B == 0 || T_q == 0) return GQA_OK;
+    return prefill::run(q, k, v, nullptr, o_part, lse_part, B, H_q, H_kv, d, T_q, S_kv, q_offset,
+                        key_offset, causal, scale, stream);
 }
 
 extern "C" int gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,

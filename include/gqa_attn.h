@@ -307,6 +307,25 @@ GQA_API int gqa_attn_prefill_ex(const uint16_t* q, const uint16_t* k, const uint
                                 int B, int H_q, int H_kv, int d, int T_q, int S_kv,
                                 int q_offset, int causal, float scale, cudaStream_t stream);
 
+/* Sequence-parallel prefill (page: ADR-0060 §5.5 prefill with SP, where the
+ * K/V slices travel between ranks, and §4 for the merge): the prefill of T_q
+ * queries at global positions q_offset + t against ONE slice of the keys, the
+ * S_kv keys at global positions key_offset + j held in the slice's own cache
+ * k, v [B, H_kv, S_kv, d]. causal != 0: query t sees key j iff
+ * key_offset + j <= q_offset + t (keys past the slice come from other
+ * slices, so q_offset + T_q may exceed key_offset + S_kv); causal == 0: every
+ * key of the slice. A row that sees no key of the slice gets O = 0 and
+ * lse = -inf. O is kept in fp32 for gqa_attn_merge over the slices (rows =
+ * B * H_q * T_q):
+ *   o_part   : fp32 [B, H_q, T_q, d], 16-byte aligned;
+ *   lse_part : fp32 [B, H_q, T_q] (required).
+ * q_offset, key_offset >= 0; other arguments and errors as
+ * gqa_attn_prefill_ex. */
+GQA_API int gqa_attn_prefill_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                     float* o_part, float* lse_part, int B, int H_q, int H_kv,
+                                     int d, int T_q, int S_kv, int q_offset, int key_offset,
+                                     int causal, float scale, cudaStream_t stream);
+
 /* ------------------------------------------------------ plan / scheduler --
  * Integer helpers the kernels use, exported so tests can compare them with
  * independent derivations bit for bit. Host-only; no GPU needed.

@@ -309,3 +309,22 @@ def test_only_the_c_abi_is_exported(L):
     ours = sorted(s[2] for s in syms if s[2].startswith("gqa_attn_"))
     assert ours == sorted(api.symbols())
     assert not [s for s in syms if "gqa" in s[2] and not s[2].startswith("gqa_attn_")]
+
+
+def test_prefill_partial_bad_args_return_codes_without_launch(L):
+    st = None
+    # q, k, v, o_part, lse_part, B, H_q, H_kv, d, T_q, S_kv, q_offset, key_offset, causal, scale
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 128, 64, 64, 0, 0, 1, 0.1)
+    bad = [((FAKE, FAKE, FAKE, FAKE, 0) + ok[5:], api.GQA_ERR_INVALID_ARG),        # lse required
+           (ok[:12] + (-1,) + ok[13:], api.GQA_ERR_INVALID_ARG),                  # key_offset
+           (ok[:11] + (-1,) + ok[12:], api.GQA_ERR_INVALID_ARG),                  # q_offset
+           (ok[:14] + (0.0,), api.GQA_ERR_INVALID_ARG),                           # scale
+           (ok[:8] + (96,) + ok[9:], api.GQA_ERR_UNSUPPORTED),                    # head dim
+           ((FAKE, FAKE, FAKE, FAKE + 8) + ok[4:], api.GQA_ERR_MISALIGNED),
+           (ok[:5] + (0,) + ok[6:], 0)]                                            # empty batch
+    for args, code in bad:
+        assert api.gqa_attn_prefill_partial(*args, st) == code, args
+    # queries past the slice's last key are allowed (the rest of the keys are
+    # in later slices); the whole-cache prefill rejects them
+    assert api.gqa_attn_prefill_ex(FAKE, FAKE, FAKE, FAKE, 0, 1, 8, 2, 128, 64, 64, 10, 1, 0.1,
+                                   st) == api.GQA_ERR_INVALID_ARG
