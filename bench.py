@@ -477,7 +477,8 @@ def run_ours(args, rank, world, local_rank):
     if have_prefill:
         # `roofline` describes the kernel with the larger share of the measured
         # step; the other one is reported beside it as roofline_<name>.
-        pk = "prefill_pair_kernel" if (p.H_q // p.H_kv) % 2 == 0 else "prefill_kernel"
+        pk = ("prefill_pair_kernel<false> (head pairs)" if (p.H_q // p.H_kv) % 2 == 0
+              else "prefill_pair_kernel<true> (block pairs)")
         roof_prefill = {
             "bound": "tensor", "achieved": pre_tflops, "peak": tc_peak, "unit": "TFLOP/s",
             "frac": pre_tflops / tc_peak, "traffic": traffic.get("prefill"), "kernel": pk,

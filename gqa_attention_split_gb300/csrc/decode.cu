@@ -19,7 +19,8 @@
 //   tiles round-robin.
 // * Tensor cores run "swapped": S^T = K_j q^T (M = 16 keys, N = 8 query heads)
 //   and O^T += V_j^T P^T (M = 16 dims, N = 8 heads), so the 8 heads of a group
-//   fill the N = 8 side of mma.m16n8k16; movmatrix turns the P^T accumulator
+//   fill the N = 8 side of mma.m16n8k16 (a group of 9-16 heads runs as two
+//   CTAs over the same K/V tiles); movmatrix turns the P^T accumulator
 //   into the B operand. Exponentials run in base 2 with log2(e)*scale folded
 //   into the scores.
 // * Level 2 of the reduction: the warps of a CTA merge in shared memory, then

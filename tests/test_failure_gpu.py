@@ -48,7 +48,7 @@ def test_inject_rejects_negative_count():
     assert api.gqa_attn_debug_inject_timeout(0) == api.GQA_OK
 
 
-@pytest.mark.parametrize("H_q,H_kv", [(16, 2), (3, 3)])  # two heads per CTA; one head per CTA
+@pytest.mark.parametrize("H_q,H_kv", [(16, 2), (3, 3)])  # head pairs; block pairs (G = 1)
 def test_prefill_timeout_is_reported_and_next_call_is_correct(H_q, H_kv):
     T, off = 300, 200
     q, k, v = wl.small_prefill(1, H_q, H_kv, 128, T, T + off, off, seed=960 + H_q)

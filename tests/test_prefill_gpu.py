@@ -55,7 +55,7 @@ def run_prefill(q, k, v, q_offset, causal, scale=None):
     (1, 8, 2, 64, 1000, 936, True),     # chunk at the end of a long prefix
     (2, 8, 4, 200, 333, 0, False),      # full attention, ragged keys
     (1, 4, 2, 1, 1, 0, True),           # a single query and key
-    (1, 6, 2, 257, 300, 43, True),      # odd G = 3 (one head per CTA), chunk at an offset
+    (1, 6, 2, 257, 300, 43, True),      # odd G = 3 (block pairs), chunk at an offset
     (1, 16, 2, 128, 640, 0, False),     # full attention over more keys than queries
     (3, 8, 1, 129, 129, 0, True),       # three batch rows, one query row past a block
     (1, 8, 2, 1, 1000, 999, True),      # one query at the end of a long prefix (causal)

@@ -136,3 +136,31 @@ def test_merge_alone_against_the_oracle_merge():
     assert (np.isneginf(lg) == ~fin).all()
     assert np.abs(lg[fin] - L[fin]).max() <= 1e-5 * np.abs(L[fin]).max() + 1e-5
     assert (o[:5] == 0).all() and torch.isneginf(lse[:5]).all()
+
+
+def test_merge_more_parts_than_a_warp_has_lanes():
+    # R > 32: the lse values are read 32 at a time; d = 128 uses float4 loads
+    g = torch.Generator().manual_seed(1201)
+    R, rows, d = 45, 70, 128
+    o_parts = torch.randn(R, rows, d, generator=g) * 0.7
+    lse_parts = torch.randn(R, rows, generator=g) * 5
+    empty = torch.rand(R, rows, generator=g) < 0.2
+    lse_parts[empty] = float("-inf")
+    o_parts[empty] = float("nan")
+    o, lse = api.merge(o_parts.cuda(), lse_parts.cuda())
+    api.check()
+    ms = lse_parts.double().numpy()
+    Os = np.where(empty.numpy()[..., None], 0.0, o_parts.double().numpy())
+    O, L = orc.combine_partials(ms, np.ones_like(ms), Os)
+    og = o.float().cpu().double().numpy()
+    assert (np.abs(og - O) <= 2.0 ** -8 * np.abs(O) + 1e-6).all()
+    assert np.abs(lse.cpu().double().numpy() - L).max() <= 1e-4
+
+
+def test_sharded_decode_group_of_16():
+    # G = 16 runs two CTAs per (split, KV head); the partials keep fp32 O
+    lens = [2500, 1200, 1]
+    q, k, v, sl = wl.small_decode(3, 32, 2, 128, 2500, seed=1202, seqlens=lens)
+    o, lse, _ = _sharded_decode(q, k, v, sl, 3)
+    O, L = orc.attention(q[:, :, None], k, v, scale=1 / math.sqrt(128), seqlens=lens)
+    _close(o.float().cpu().numpy(), lse.cpu().numpy(), O[:, :, 0], L[:, :, 0], "G=16 R=3")
