@@ -327,7 +327,7 @@ def run_ours(args, rank, world, local_rank):
         decode_layers()
     kv_b, alg_b = decode_bytes(w.B, w.H_q, w.H_kv, w.d, sl0.tolist())
 
-    # ---- prefill: one 8K causal call (if the kernel is in this build)
+    # ---- prefill: one 8K causal call (if the library has the prefill kernel)
     p = wl.CAUSAL_PREFILL_8K
     qp, kp, vp = (t.to(dev) for t in wl.prefill_inputs(p))
     op = torch.empty_like(qp)
