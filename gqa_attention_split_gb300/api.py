@@ -60,9 +60,11 @@ _SIGNATURES = {
     "gqa_attn_prefill_tile_counts": (_I, [_I, _I, _I, _I, _P, _P, _P]),
     "gqa_attn_prefill_block_m": (_I, []),
     "gqa_attn_prefill_block_n": (_I, []),
+    "gqa_attn_prefill_schedule": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I]),
     "gqa_attn_check": (_I, [_P]),
     "gqa_attn_debug_inject_timeout": (_I, [_I]),
     "gqa_attn_debug_tile_counts": (_I, [_P, _I]),
+    "gqa_attn_debug_prefill_order": (_I, [ctypes.c_int64]),
     "gqa_attn_strerror": (ctypes.c_char_p, [_I]),
     "gqa_attn_version": (_I, []),
 }
@@ -208,12 +210,28 @@ def gqa_attn_prefill_block_n():
     return lib().gqa_attn_prefill_block_n()
 
 
+def gqa_attn_prefill_schedule(B, H_q, H_kv, d, T_q, S_kv, q_offset, causal, num_ctas,
+                              item_cap=12288):
+    """Returns (rc, per-CTA item lists); rc = 0 (closed-form order) gives []."""
+    off = (ctypes.c_int32 * (num_ctas + 1))()
+    items = (ctypes.c_int32 * max(1, item_cap))()
+    rc = lib().gqa_attn_prefill_schedule(B, H_q, H_kv, d, T_q, S_kv, q_offset, causal, num_ctas,
+                                         off, items, item_cap)
+    if rc <= 0:
+        return rc, []
+    return rc, [list(items[off[c]:off[c + 1]]) for c in range(num_ctas)]
+
+
 def gqa_attn_check(stream=None):
     return lib().gqa_attn_check(stream)
 
 
 def gqa_attn_debug_inject_timeout(launches):
     return lib().gqa_attn_debug_inject_timeout(launches)
+
+
+def gqa_attn_debug_prefill_order(budget_bytes):
+    return lib().gqa_attn_debug_prefill_order(budget_bytes)
 
 
 def gqa_attn_debug_tile_counts(clear=False, L=None):

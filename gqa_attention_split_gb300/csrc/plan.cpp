@@ -7,9 +7,17 @@
 //   §2.2 valid-length arithmetic  -> split bounds (contiguous chunks here)
 //   §5.4 prefill tile classes     -> gqa_attn_tile_class
 //   §9 tuning (split/tile sizes)  -> gqa_attn_pick_num_splits
+//   §5.4 prefill scheduling       -> plan_prefill_order (work order of the
+//                                    persistent prefill kernel)
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
+#include <functional>
+#include <memory>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "gqa_attn.h"
 #include "plan.cuh"
@@ -105,5 +113,136 @@ extern "C" int gqa_attn_prefill_tile_counts(int T_q, int S_kv, int q_offset, int
     *n_past = c[gqa::kTileAllPast];
     *n_partial = c[gqa::kTilePartial];
     *n_future = c[gqa::kTileAllFuture];
+    return GQA_OK;
+}
+
+namespace gqa {
+
+namespace {
+
+std::atomic<int64_t> g_order_budget{-1};  // < 0: kPrefillL2Budget
+
+// The prefill kernel's item numbering (pair_item in prefill.cu), host side:
+// item L's (batch, KV head) group and the KV tiles it runs.
+struct ItemShape {
+    int group;
+    int n;
+};
+
+ItemShape prefill_item(int B, int H_q, int H_kv, int T_q, int S_kv, int q_offset, bool causal,
+                       bool partial, bool blocks, int64_t L) {
+    const int G = H_q / H_kv, BM = kPrefillBlockM, BN = kPrefillBlockN;
+    const int tiles = int(ceil_div(S_kv, BN)), n_mblocks = int(ceil_div(T_q, BM));
+    auto block_tiles = [&](int row0) {
+        if (row0 >= T_q) return 0;
+        const int qe = q_offset + std::min(row0 + BM, T_q);
+        if (!causal) return tiles;
+        if (partial && qe <= 0) return 0;  // the slice starts past these queries
+        return std::min(tiles, (qe - 1) / BN + 1);
+    };
+    ItemShape r{};
+    if (blocks) {  // two consecutive query blocks of one head
+        const int64_t bh_count = int64_t(B) * H_q;
+        const int bpi = int((n_mblocks + 1) / 2 - 1 - L / bh_count);
+        const int bh = int(L % bh_count), b = bh / H_q, h = bh % H_q;
+        r.group = b * H_kv + h / G;
+        r.n = std::max(block_tiles(2 * bpi * BM), block_tiles((2 * bpi + 1) * BM));
+    } else {  // one query block of two heads
+        const int pairs = H_q / 2;
+        const int64_t bp_count = int64_t(B) * pairs;
+        const int m = int(n_mblocks - 1 - L / bp_count), bp = int(L % bp_count);
+        const int b = bp / pairs, h = (bp % pairs) * 2;
+        r.group = b * H_kv + h / G;
+        r.n = block_tiles(m * BM);
+    }
+    return r;
+}
+
+}  // namespace
+
+int64_t prefill_order_budget() {
+    const int64_t b = g_order_budget.load(std::memory_order_relaxed);
+    return b < 0 ? kPrefillL2Budget : b;
+}
+
+bool plan_prefill_order(PrefillSched& s, int B, int H_q, int H_kv, int d, int T_q, int S_kv,
+                        int q_offset, bool causal, bool partial, int ctas, int64_t items,
+                        int64_t l2_budget) {
+    s.on = 0;
+    if (l2_budget <= 0 || ctas <= 0 || ctas > kPrefillSchedCtas || items <= 0 ||
+        items > kPrefillSchedItems || B <= 0 || H_kv <= 0 || H_q % H_kv != 0 || S_kv <= 0)
+        return false;
+    const int64_t group_bytes = int64_t(S_kv) * d * 2 * 2;  // K and V rows, bf16
+    const int64_t groups = int64_t(B) * H_kv;
+    if (group_bytes * groups <= l2_budget) return false;  // all of K/V stays in L2
+    // n_sg super-groups whose sizes differ by at most one group (a small last
+    // one would end the launch on its heaviest items): group g is in
+    // super-group g * n_sg / groups
+    const int64_t sg_max = std::max<int64_t>(1, l2_budget / group_bytes);
+    const int64_t n_sg = ceil_div(groups, sg_max);
+    const bool blocks = (H_q / H_kv) % 2 != 0;
+    struct Key {
+        int64_t sg;
+        int n;
+        int L;
+    };
+    std::vector<Key> keys(static_cast<size_t>(items));
+    for (int64_t L = 0; L < items; ++L) {
+        const ItemShape it = prefill_item(B, H_q, H_kv, T_q, S_kv, q_offset, causal, partial,
+                                          blocks, L);
+        keys[size_t(L)] = Key{int64_t(it.group) * n_sg / groups, it.n, int(L)};
+    }
+    std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
+        if (a.sg != b.sg) return a.sg < b.sg;
+        if (a.n != b.n) return a.n > b.n;
+        return a.L < b.L;
+    });
+    // greedy: the next item to the CTA with the least work so far (ties: the
+    // lowest CTA index); an item costs its KV tiles plus about one tile of
+    // Q load and epilogue
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> free_at;
+    for (int c = 0; c < ctas; ++c) free_at.push({0, c});
+    std::vector<std::vector<uint16_t>> per(static_cast<size_t>(ctas));
+    for (const Key& k : keys) {
+        const Load t = free_at.top();
+        free_at.pop();
+        per[size_t(t.second)].push_back(uint16_t(k.L));
+        free_at.push({t.first + k.n + 1, t.second});
+    }
+    int at = 0;
+    for (int c = 0; c < ctas; ++c) {
+        s.off[c] = uint16_t(at);
+        for (uint16_t L : per[size_t(c)]) s.item[at++] = L;
+    }
+    s.off[ctas] = uint16_t(at);
+    s.on = 1;
+    return true;
+}
+
+}  // namespace gqa
+
+extern "C" int gqa_attn_prefill_schedule(int B, int H_q, int H_kv, int d, int T_q, int S_kv,
+                                         int q_offset, int causal, int num_ctas, int32_t* off,
+                                         int32_t* items, int item_cap) {
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0 || T_q < 0 || S_kv <= 0 ||
+        num_ctas <= 0 || !off || !items || item_cap < 0)
+        return GQA_ERR_INVALID_ARG;
+    const bool blocks = (H_q / H_kv) % 2 != 0;
+    const int64_t n_mblocks = ceil_div(T_q, gqa::kPrefillBlockM);
+    const int64_t n_items = blocks ? (n_mblocks + 1) / 2 * B * H_q : n_mblocks * B * (H_q / 2);
+    auto s = std::make_unique<gqa::PrefillSched>();
+    if (!gqa::plan_prefill_order(*s, B, H_q, H_kv, d, T_q, S_kv, q_offset, causal != 0, false,
+                                 num_ctas, n_items, gqa::prefill_order_budget()))
+        return 0;
+    const int n = s->off[num_ctas];
+    if (n > item_cap) return GQA_ERR_INVALID_ARG;
+    for (int c = 0; c <= num_ctas; ++c) off[c] = s->off[c];
+    for (int i = 0; i < n; ++i) items[i] = s->item[i];
+    return n;
+}
+
+extern "C" int gqa_attn_debug_prefill_order(int64_t budget_bytes) {
+    gqa::g_order_budget.store(budget_bytes < 0 ? -1 : budget_bytes, std::memory_order_relaxed);
     return GQA_OK;
 }

@@ -60,4 +60,37 @@ inline int decode_cluster_size(int ns, int64_t ctas, int num_sms) {
     return 1;
 }
 
+// Work order of the persistent prefill kernel, passed as a kernel parameter.
+// With on == 0 the kernel walks its closed-form order (heaviest query blocks
+// first over every batch and KV head, snake order over the CTAs). When the
+// K/V of all (batch, KV head) groups is larger than L2 that order streams
+// every group's keys from DRAM again in each round of items; the host then
+// orders the items by super-groups of (batch, KV head) whose K/V fits in an
+// L2 budget, heaviest first within a super-group, and gives each item to the
+// CTA with the least work so far. CTA c runs item[off[c]] .. item[off[c+1]-1]
+// (the kernel's own item numbers). The order changes no result: items are
+// independent and each is computed the same way wherever it runs.
+constexpr int kPrefillSchedCtas = 160;
+constexpr int kPrefillSchedItems = 12288;
+// K/V bytes per super-group: two neighbouring super-groups (the CTAs move
+// from one to the next at different times) stay within the 129 MB L2
+constexpr int64_t kPrefillL2Budget = int64_t(48) << 20;
+
+struct PrefillSched {
+    int on;
+    uint16_t off[kPrefillSchedCtas + 1];
+    uint16_t item[kPrefillSchedItems];
+};
+
+// Fills `s` for a launch of `ctas` CTAs over `items` work items (s.on = 0 and
+// false when the closed-form order is kept). q_offset is relative to the first
+// key of the launch; partial: a slice launch, whose blocks may see no key.
+// l2_budget: K/V bytes per super-group (<= 0: always the closed-form order).
+bool plan_prefill_order(PrefillSched& s, int B, int H_q, int H_kv, int d, int T_q, int S_kv,
+                        int q_offset, bool causal, bool partial, int ctas, int64_t items,
+                        int64_t l2_budget);
+
+// The budget the library uses (test hook: gqa_attn_debug_prefill_order).
+int64_t prefill_order_budget();
+
 }  // namespace gqa

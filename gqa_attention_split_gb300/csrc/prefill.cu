@@ -22,6 +22,12 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <array>
+#include <memory>
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "gqa_attn.h"
 #include "plan.cuh"
 #include "ptx.cuh"
@@ -179,7 +185,8 @@ static_assert(pNumBars * 8 + 4 <= 256, "barrier area");
 // Even G: one query block of two adjacent query heads of a KV group. Odd G
 // (pair_blocks): two consecutive query blocks of one head. Items are numbered
 // heaviest first (query blocks from the last one down), and a CTA takes items
-// c, 2G-1-c, 2G+c, ... (snake order). Each group has its own KV tile count
+// c, 2G-1-c, 2G+c, ... (snake order), or the items a host-made order
+// (PrefillSched, plan.cuh) lists for it. Each group has its own KV tile count
 // (causal: up to its own last query), possibly 0 (the second block of a head
 // with an odd block count); the item runs the larger one.
 struct PairItem {
@@ -199,9 +206,17 @@ struct PairItem {
 // kPartial: a prefill over one slice of the keys, where the query offset
 // relative to the slice may be negative and a block may see no key (n = 0).
 template <bool kBlocks, bool kPartial>
-__device__ __forceinline__ bool pair_item(const Params& p, int it, PairItem& w) {
+__device__ __forceinline__ bool pair_item(const Params& p, const PrefillSched& sch, int it,
+                                          PairItem& w) {
     const int G = gridDim.x, c = blockIdx.x;
-    const int L = it * G + ((it & 1) ? G - 1 - c : c);
+    int L;
+    if (sch.on) {
+        const int i = sch.off[c] + it;
+        if (i >= sch.off[c + 1]) return false;
+        L = sch.item[i];
+    } else {
+        L = it * G + ((it & 1) ? G - 1 - c : c);
+    }
     int h;
     if constexpr (kBlocks) {
         const int tiles = (p.S_kv + BN - 1) / BN;
@@ -258,7 +273,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
-                        const __grid_constant__ CUtensorMap tmap_o, const Params p) {
+                        const __grid_constant__ CUtensorMap tmap_o, const Params p,
+                        const __grid_constant__ PrefillSched sched) {
     using Gm = PairGeo<D>;
     constexpr uint32_t kTileBytes = Gm::kTileBytes;
     // per-group bookkeeping: block pairs, or slices where a group may see no key
@@ -307,7 +323,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         bool alive = true;
         int r = 0;        // ring items issued so far, over all work items
         int q_loads = 0;  // Q loads issued (one per work item)
-        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, sched, it, w); ++it) {
             // Q of both heads; the previous item's last S MMAs must be done.
             if (it > 0) alive = mbar_wait_bounded(bar(pQEmpty), (it - 1) & 1, p.status);
             if (!alive) break;
@@ -387,7 +403,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         int r = 0;                // ring items consumed so far
         int tt[2] = {0, 0};       // KV tiles group g finished so far (its S and P phases)
         GQA_DBG(unsigned long long dbg[3] = {0, 0, 0};)
-        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, sched, it, w); ++it) {
             const int n = w.n_tiles;
             if constexpr (kPartial) {
                 if (n == 0) {  // no group sees a key of this slice: Q is free again
@@ -502,7 +518,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         bool alive = true;
         int tt = 0;   // KV tiles this group finished so far, over all work items
         [[maybe_unused]] int itg = 0;  // block pairs: items in which this group had tiles
-        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, it, w); ++it) {
+        for (int it = 0; alive && pair_item<kBlocks, kPartial>(p, sched, it, w); ++it) {
             // this group's fields (selected, not indexed: they stay in registers)
             const int ng = kGen ? (g ? w.n[1] : w.n[0]) : w.n_tiles;
             if constexpr (kGen) {
@@ -743,7 +759,8 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
 // device.
 template <bool kBlocks, int D, bool kPartial>
 int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                const CUtensorMap& to, const Params& prm, int ctas, cudaStream_t stream) {
+                const CUtensorMap& to, const Params& prm, const PrefillSched& sched, int ctas,
+                cudaStream_t stream) {
     auto kern = prefill_pair_kernel<kBlocks, D, kPartial>;
     static std::atomic<uint64_t> attr_done{0};
     const int dev = current_device();
@@ -754,8 +771,43 @@ int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap&
         device_attrs_mark(attr_done, dev);
     }
     kern<<<dim3(unsigned(ctas)), kPairThreads, PairGeo<D>::kSmemBytes, stream>>>(tq, tk, tv, to,
-                                                                                prm);
+                                                                                prm, sched);
     return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+// The work order of a launch (plan_prefill_order), cached per shape: a
+// model's layers repeat a few shapes, and the plan sorts every item. The
+// kernel parameter is copied at launch, so a plan only has to outlive the
+// launch call.
+std::shared_ptr<const PrefillSched> work_order(int B, int H_q, int H_kv, int d, int T_q,
+                                               int S_kv, int q_offset, bool causal, bool partial,
+                                               int ctas, int64_t items) {
+    // (no make_shared: its type tag is a process-unique symbol that the
+    // dynamic linker would merge across libraries)
+    static const std::shared_ptr<const PrefillSched> closed_form(new PrefillSched{});
+    const int64_t budget = prefill_order_budget();
+    const int64_t groups = int64_t(B) * H_kv, group_bytes = int64_t(S_kv) * d * 4;
+    if (budget <= 0 || group_bytes * groups <= budget || items > kPrefillSchedItems ||
+        ctas > kPrefillSchedCtas)
+        return closed_form;
+    using Key = std::array<int64_t, 12>;
+    const Key key{B, H_q, H_kv, d, T_q, S_kv, q_offset, causal, partial, ctas, items, budget};
+    static std::mutex mu;
+    static std::vector<std::pair<Key, std::shared_ptr<const PrefillSched>>> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const auto& e : cache)
+            if (e.first == key) return e.second;
+    }
+    std::shared_ptr<PrefillSched> s(new PrefillSched{});
+    if (!plan_prefill_order(*s, B, H_q, H_kv, d, T_q, S_kv, q_offset, causal, partial, ctas,
+                            items, budget))
+        return closed_form;
+    std::shared_ptr<const PrefillSched> plan(std::move(s));
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() >= 16) cache.erase(cache.begin());  // oldest first
+    cache.emplace_back(key, plan);
+    return plan;
 }
 
 // Both entry points: queries at global positions q_offset + t against keys
@@ -803,22 +855,26 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
     const int sms = num_sms();
     if (sms <= 0) return GQA_ERR_CUDA;
     const int ctas = int(items < int64_t(sms) ? items : int64_t(sms));
+    const std::shared_ptr<const PrefillSched> sched =
+        work_order(B, H_q, H_kv, d, T_q, S_kv, prm.q_offset, causal != 0, partial, ctas, items);
+    if (!sched) return GQA_ERR_CUDA;
+    const PrefillSched& ord = *sched;
     if (partial) {  // O leaves through plain fp32 stores; the O map is not read
         to = tq;
         if (d == 128)
-            return blocks ? launch_pair<true, 128, true>(tq, tk, tv, to, prm, ctas, stream)
-                          : launch_pair<false, 128, true>(tq, tk, tv, to, prm, ctas, stream);
-        return blocks ? launch_pair<true, 64, true>(tq, tk, tv, to, prm, ctas, stream)
-                      : launch_pair<false, 64, true>(tq, tk, tv, to, prm, ctas, stream);
+            return blocks ? launch_pair<true, 128, true>(tq, tk, tv, to, prm, ord, ctas, stream)
+                          : launch_pair<false, 128, true>(tq, tk, tv, to, prm, ord, ctas, stream);
+        return blocks ? launch_pair<true, 64, true>(tq, tk, tv, to, prm, ord, ctas, stream)
+                      : launch_pair<false, 64, true>(tq, tk, tv, to, prm, ord, ctas, stream);
     }
     if (encode_tmap_3d_bf16(&to, o, d, T_q, uint64_t(B) * H_q, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess)
         return GQA_ERR_CUDA;
     if (d == 128)
-        return blocks ? launch_pair<true, 128, false>(tq, tk, tv, to, prm, ctas, stream)
-                      : launch_pair<false, 128, false>(tq, tk, tv, to, prm, ctas, stream);
-    return blocks ? launch_pair<true, 64, false>(tq, tk, tv, to, prm, ctas, stream)
-                  : launch_pair<false, 64, false>(tq, tk, tv, to, prm, ctas, stream);
+        return blocks ? launch_pair<true, 128, false>(tq, tk, tv, to, prm, ord, ctas, stream)
+                      : launch_pair<false, 128, false>(tq, tk, tv, to, prm, ord, ctas, stream);
+    return blocks ? launch_pair<true, 64, false>(tq, tk, tv, to, prm, ord, ctas, stream)
+                  : launch_pair<false, 64, false>(tq, tk, tv, to, prm, ord, ctas, stream);
 }
 
 }  // namespace prefill

@@ -381,6 +381,26 @@ GQA_API int gqa_attn_prefill_tile_counts(int T_q, int S_kv, int q_offset, int ca
 GQA_API int gqa_attn_prefill_block_m(void);
 GQA_API int gqa_attn_prefill_block_n(void);
 
+/* Work order of a prefill launch (page: ADR-0060 §5.4 prefill scheduling;
+ * the kernel is persistent, one CTA per SM over all work items). A work item
+ * is one query block of two query heads of a KV group (even G) or two
+ * consecutive query blocks of one head (odd G). When the K and V rows of all
+ * B * H_kv groups are larger than an L2 budget (48 MiB), the items are
+ * ordered by super-groups of (batch, KV head) whose K/V fits in the budget
+ * (n_sg = ceil(groups / max(1, floor(budget / group bytes))) super-groups;
+ * group g in super-group g * n_sg / groups),
+ * heaviest first within a super-group, and each goes to the CTA with the
+ * least work so far (item cost: its KV tiles + 1), so that concurrently
+ * running CTAs share their keys in L2; otherwise the kernel's closed-form
+ * order runs. Host-only: writes off[0..num_ctas] and items[0..off[num_ctas])
+ * (CTA c runs items[off[c]] .. items[off[c+1]-1], in the kernel's own item
+ * numbers) and returns the number of items, or 0 when the closed-form order is
+ * kept (nothing written) or the table does not fit (more than 12288 items or
+ * 160 CTAs). item_cap bounds `items`. Errors: GQA_ERR_INVALID_ARG. */
+GQA_API int gqa_attn_prefill_schedule(int B, int H_q, int H_kv, int d, int T_q, int S_kv,
+                                      int q_offset, int causal, int num_ctas, int32_t* off,
+                                      int32_t* items, int item_cap);
+
 /* ------------------------------------------------------------ status ----- */
 
 /* Synchronises `stream`, then reads and clears the device status word of the
@@ -409,6 +429,14 @@ GQA_API int gqa_attn_debug_inject_timeout(int launches);
  * clear != 0. A correct schedule issues no all-future tile. Other builds
  * return GQA_ERR_UNSUPPORTED and touch nothing. */
 GQA_API int gqa_attn_debug_tile_counts(int64_t* counts, int clear);
+
+/* Test hook for the prefill work order (see gqa_attn_prefill_schedule):
+ * budget_bytes < 0 restores the library's 48 MiB L2 budget; 0 keeps the
+ * closed-form order for every launch; > 0 uses that budget (a small one makes
+ * even tiny problems run a host-made order of one group per super-group).
+ * Applies to later calls of gqa_attn_prefill* and gqa_attn_prefill_schedule.
+ * Returns GQA_OK. */
+GQA_API int gqa_attn_debug_prefill_order(int64_t budget_bytes);
 
 /* Static, human-readable text for a return code. */
 GQA_API const char* gqa_attn_strerror(int code);
