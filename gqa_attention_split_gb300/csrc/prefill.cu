@@ -667,22 +667,41 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const bool valid = row0_g + row < p.T_q;
             const size_t orow = (size_t(w.b) * p.H_q + head_g) * p.T_q + row0_g + row;
             if constexpr (kPartial) {
-                // fp32 O for the merge, row by row; a row that saw no key of the
-                // slice gets O = 0 and lse = -inf
+                // fp32 O for the merge, through the same staging buffers and TMA
+                // stores as bf16: a chunk is 16 fp32 columns, 64 B per row like
+                // 32 bf16 columns. A row that saw no key of the slice gets O = 0
+                // and lse = -inf.
                 const float inv = lb_run > 0.f ? 1.f / lb_run : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     tc::tmem_ld32(lane_base + col_o + c * 32, r);
                     tc::tmem_wait_ld();
-                    if (valid) {
-                        float4* dst = reinterpret_cast<float4*>(p.o32 + orow * D + c * 32);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv,
-                                                 __uint_as_float(r[4 * i + 1]) * inv,
-                                                 __uint_as_float(r[4 * i + 2]) * inv,
-                                                 __uint_as_float(r[4 * i + 3]) * inv);
+                    for (int h = 0; h < 2; ++h) {
+                        const int chunk = 2 * c + h;
+                        // buffer chunk & 1 was last read by the store two chunks back
+                        const uint32_t buf = stage + (chunk & 1) * kStageBoxBytes;
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const int i = h * 16 + v4 * 4;
+                            uint4 o4;
+                            o4.x = __float_as_uint(__uint_as_float(r[i]) * inv);
+                            o4.y = __float_as_uint(__uint_as_float(r[i + 1]) * inv);
+                            o4.z = __float_as_uint(__uint_as_float(r[i + 2]) * inv);
+                            o4.w = __float_as_uint(__uint_as_float(r[i + 3]) * inv);
+                            st_shared_v4(buf + lane * 64 + ((v4 ^ ((lane >> 1) & 3)) << 4), o4);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            // rows at or past T_q fall outside the tensor, not written
+                            tma_store_3d(&tmap_o, buf, chunk * 16, row0_g + quad * 32,
+                                         w.b * p.H_q + head_g);
+                            bulk_commit_group();
+                        }
                     }
                 }
                 if (valid)
@@ -859,8 +878,12 @@ int run(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, fl
         work_order(B, H_q, H_kv, d, T_q, S_kv, prm.q_offset, causal != 0, partial, ctas, items);
     if (!sched) return GQA_ERR_CUDA;
     const PrefillSched& ord = *sched;
-    if (partial) {  // O leaves through plain fp32 stores; the O map is not read
-        to = tq;
+    if (partial) {  // fp32 O: boxes of 16 columns x 32 rows (64 B rows, as bf16's 32 columns)
+        const uint64_t od[3] = {uint64_t(d), uint64_t(T_q), uint64_t(B) * H_q};
+        const uint32_t ob[3] = {16, 32, 1};
+        if (encode_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 3, o32, od, ob,
+                        CU_TENSOR_MAP_SWIZZLE_64B) != cudaSuccess)
+            return GQA_ERR_CUDA;
         if (d == 128)
             return blocks ? launch_pair<true, 128, true>(tq, tk, tv, to, prm, ord, ctas, stream)
                           : launch_pair<false, 128, true>(tq, tk, tv, to, prm, ord, ctas, stream);
