@@ -225,9 +225,14 @@ bool plan_prefill_order(PrefillSched& s, int B, int H_q, int H_kv, int d, int T_
 extern "C" int gqa_attn_prefill_schedule(int B, int H_q, int H_kv, int d, int T_q, int S_kv,
                                          int q_offset, int causal, int num_ctas, int32_t* off,
                                          int32_t* items, int item_cap) {
-    if (B <= 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0 || T_q < 0 || S_kv <= 0 ||
-        num_ctas <= 0 || !off || !items || item_cap < 0)
+    // the prefill entry points' own limits
+    if (B <= 0 || B > 65535 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || T_q < 0 ||
+        S_kv <= 0 || q_offset < 0 || num_ctas <= 0 || !off || !items || item_cap < 0)
         return GQA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+    if (int64_t(B) * H_q * T_q >= (int64_t(1) << 31) ||
+        int64_t(B) * H_kv * S_kv >= (int64_t(1) << 31))
+        return GQA_ERR_UNSUPPORTED;
     const bool blocks = (H_q / H_kv) % 2 != 0;
     const int64_t n_mblocks = ceil_div(T_q, gqa::kPrefillBlockM);
     const int64_t n_items = blocks ? (n_mblocks + 1) / 2 * B * H_q : n_mblocks * B * (H_q / 2);

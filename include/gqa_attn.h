@@ -396,7 +396,9 @@ GQA_API int gqa_attn_prefill_block_n(void);
  * (CTA c runs items[off[c]] .. items[off[c+1]-1], in the kernel's own item
  * numbers) and returns the number of items, or 0 when the closed-form order is
  * kept (nothing written) or the table does not fit (more than 12288 items or
- * 160 CTAs). item_cap bounds `items`. Errors: GQA_ERR_INVALID_ARG. */
+ * 160 CTAs). item_cap bounds `items`. Errors: GQA_ERR_INVALID_ARG (bad sizes,
+ * q_offset < 0, null pointers, item_cap too small), GQA_ERR_UNSUPPORTED (d not
+ * in {64, 128}, or a shape the prefill entry points reject). */
 GQA_API int gqa_attn_prefill_schedule(int B, int H_q, int H_kv, int d, int T_q, int S_kv,
                                       int q_offset, int causal, int num_ctas, int32_t* off,
                                       int32_t* items, int item_cap);

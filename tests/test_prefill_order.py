@@ -143,6 +143,12 @@ def test_limits_and_errors():
         == api.GQA_ERR_INVALID_ARG                     # H_q not a multiple of H_kv
     assert api.gqa_attn_prefill_schedule(1, 64, 8, 128, 128, 128, 0, 1, 0)[0] \
         == api.GQA_ERR_INVALID_ARG
+    assert api.gqa_attn_prefill_schedule(1, 64, 8, 96, 2048, 32768, 0, 1, 152)[0] \
+        == api.GQA_ERR_UNSUPPORTED                     # d not 64 or 128
+    assert api.gqa_attn_prefill_schedule(1, 64, 8, 128, 2048, 1 << 29, 0, 1, 152)[0] \
+        == api.GQA_ERR_UNSUPPORTED                     # B * H_kv * S_kv >= 2^31
+    assert api.gqa_attn_prefill_schedule(1, 64, 8, 128, 2048, 32768, -1, 1, 152)[0] \
+        == api.GQA_ERR_INVALID_ARG
     # an item_cap smaller than the plan
     assert api.gqa_attn_prefill_schedule(2, 64, 8, 128, 2048, 32768, 30720, 1, 152,
                                          item_cap=100)[0] == api.GQA_ERR_INVALID_ARG
