@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kMinKeysPerSplit = 256;   // below this a split is mostly ramp-up
 constexpr int kMaxKeysPerSplit = 1024;  // long rows spread over many blocks
+constexpr int kMaxKeysPerWaveSplit = 2048;  // split bound of the one-wave plan below
 constexpr int kMaxSplits = 8192;
 constexpr int kClusterSplits = 16;      // splits merged on chip by one thread-block cluster
 
@@ -36,7 +37,21 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 extern "C" int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms) {
     if (B <= 0 || H_kv <= 0 || S_max <= 0 || num_sms <= 0) return GQA_ERR_INVALID_ARG;
     const int64_t pairs = int64_t(B) * H_kv;
-    // Enough blocks to cover the SMs at low batch, in whole clusters of
+    // One wave of whole-row clusters: the largest ns of 16, 8, 4, 2 whose
+    // grid fits on the SMs, if it keeps >= 80% of them busy and its splits
+    // hold 256..2048 keys. Each row then merges on chip in one cluster and no
+    // combine kernel runs (GB300, 64/8 heads: B = 2 at 8K 13.9 us with 8
+    // splits against 19.6 with 10; B = 1 at 32K 24.3 us with 16 against 28.0
+    // with 32).
+    for (int ns : {16, 8, 4, 2}) {
+        if (pairs * ns > num_sms) continue;
+        const int64_t keys = ceil_div(S_max, ns);
+        if (5 * pairs * ns >= 4 * int64_t(num_sms) && keys >= kMinKeysPerSplit &&
+            keys <= kMaxKeysPerWaveSplit)
+            return ns;
+        break;
+    }
+    // Otherwise enough blocks to cover the SMs at low batch, in whole clusters of
     // kClusterSplits splits once a row gets that many (the decode kernel
     // merges one cluster's splits on chip).
     int64_t ns = ceil_div(num_sms, pairs);

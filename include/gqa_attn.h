@@ -331,11 +331,14 @@ GQA_API int gqa_attn_prefill_partial(const uint16_t* q, const uint16_t* k, const
  * independent derivations bit for bit. Host-only; no GPU needed.
  */
 
-/* Split count for a decode problem: n = ceil(num_sms / (B * H_kv)) blocks per
- * row (when above 16, rounded down to a multiple of 16 if the blocks then
- * still cover >= 80% of the SMs), at least
- * ceil(S_max / 1024) (rounded up to a multiple of 16 when above 16), and at
- * most max(1, S_max / 256) so no split is shorter than 256 keys. Returns
+/* Split count for a decode problem. First, one wave of whole-row clusters:
+ * the largest n of 16, 8, 4, 2 with B * H_kv * n <= num_sms, taken if
+ * B * H_kv * n >= 0.8 * num_sms and 256 <= ceil(S_max / n) <= 2048 (every
+ * row then merges on chip, with no combine kernel). Otherwise
+ * n = ceil(num_sms / (B * H_kv)) blocks per row (when above 16, rounded down
+ * to a multiple of 16 if the blocks then still cover >= 80% of the SMs), at
+ * least ceil(S_max / 1024) (rounded up to a multiple of 16 when above 16), and
+ * at most max(1, S_max / 256) so no split is shorter than 256 keys. Returns
  * >= 1, or GQA_ERR_INVALID_ARG. */
 GQA_API int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
 

@@ -88,6 +88,11 @@ def test_prefill_tile_counts_bit_exact_vs_oracle(L, T_q, S_kv, off, causal):
 def _pick_reference(B, H_kv, S, sms):
     # The rule stated in include/gqa_attn.h, restated independently.
     cdiv = lambda a, b: -(-a // b)
+    fits = [n for n in (16, 8, 4, 2) if B * H_kv * n <= sms]
+    if fits:   # one wave of whole-row clusters, if it is busy enough
+        n = fits[0]
+        if B * H_kv * n >= 0.8 * sms and 256 <= cdiv(S, n) <= 2048:
+            return n
     n = cdiv(sms, B * H_kv)
     if n > 16 and B * H_kv * 16 * (n // 16) >= 0.8 * sms:
         n = 16 * (n // 16)
@@ -101,8 +106,12 @@ def test_pick_num_splits_bit_exact_and_properties(L):
     assert api.gqa_attn_pick_num_splits(1, 8, 8192, 152) == 16       # 8K decode: 8 clusters
     assert api.gqa_attn_pick_num_splits(4, 8, 131072, 152) == 128    # 128K ragged decode
     assert api.gqa_attn_pick_num_splits(1, 1, 256, 152) == 1         # tiny decode
-    for B, H_kv, S, sms in itertools.product((1, 2, 3, 4, 64), (1, 2, 8),
-                                             (1, 255, 256, 1000, 8192, 100000, 131072),
+    assert api.gqa_attn_pick_num_splits(2, 8, 8192, 152) == 8        # one wave, 8 clusters of 8
+    assert api.gqa_attn_pick_num_splits(1, 8, 32768, 152) == 16      # one wave, 2048-key splits
+    assert api.gqa_attn_pick_num_splits(1, 8, 65536, 152) == 64      # 4096-key splits: no
+    for B, H_kv, S, sms in itertools.product((1, 2, 3, 4, 8, 64), (1, 2, 8),
+                                             (1, 255, 256, 1000, 2048, 4096, 8192, 16384,
+                                              32768, 100000, 131072),
                                              (1, 148, 152)):
         ns = api.gqa_attn_pick_num_splits(B, H_kv, S, sms)
         assert ns == _pick_reference(B, H_kv, S, sms), (B, H_kv, S, sms)
