@@ -1145,6 +1145,28 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // CTAs of a decode launch: one per (split, KV head, batch row), times the
 // groups of at most kMaxG query heads a KV head's group splits into.
+// num_splits = 0: the plan `pick` (gqa_attn_pick_num_splits or its INT8 / INT4
+// forms). A bf16 group of more than 8 query heads runs as two CTAs per split
+// and KV head that read the same keys: the plan for 2 * H_kv heads (the CTAs
+// the launch has) is taken when it is one wave of splits of at most 1024 keys,
+// else the plan for H_kv heads (GB300, 128/8 heads at 8K: B = 1 12.7 us with
+// 8 splits against 14.6 with 16; B = 2 18.5 us with 8 against 21.8 with 4,
+// where the shared reads make the SMs' intake the bound). Returns the split
+// count, or a negative error code.
+int auto_splits(int (*pick)(int, int, int, int), int B, int H_q, int H_kv, int S_max) {
+    const int sms = num_sms();
+    if (sms <= 0) return GQA_ERR_CUDA;
+    int ns = -1;
+    if (H_q / H_kv > kMaxG && pick == gqa_attn_pick_num_splits) {
+        const int ns2 = pick(B, 2 * H_kv, S_max, sms);
+        if (ns2 >= 1 && int64_t(B) * 2 * H_kv * ns2 <= sms &&
+            (int64_t(S_max) + ns2 - 1) / ns2 <= 1024)
+            ns = ns2;
+    }
+    if (ns < 1) ns = pick(B, H_kv, S_max, sms);
+    return ns < 1 ? GQA_ERR_INVALID_ARG : ns;
+}
+
 int64_t grid_ctas(int ns, int B, int H_q, int H_kv) {
     const int G = H_q / H_kv;
     return int64_t(ns) * H_kv * B * ((G + kMaxG - 1) / kMaxG);
@@ -1433,10 +1455,8 @@ extern "C" int gqa_attn_decode(const uint16_t* q, const uint16_t* k, const uint1
     if (B == 0) return GQA_OK;
     int ns = num_splits;
     if (ns == 0) {
-        const int sms = num_sms();
-        if (sms <= 0) return GQA_ERR_CUDA;
-        ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
-        if (ns < 1) return GQA_ERR_INVALID_ARG;
+        ns = decode::auto_splits(gqa_attn_pick_num_splits, B, H_q, H_kv, S_max);
+        if (ns < 1) return ns;
     }
     const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
@@ -1525,10 +1545,8 @@ extern "C" int gqa_attn_decode_partial(const uint16_t* q, const uint16_t* k, con
     if (B == 0) return GQA_OK;
     int ns = num_splits;
     if (ns == 0) {
-        const int sms = num_sms();
-        if (sms <= 0) return GQA_ERR_CUDA;
-        ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
-        if (ns < 1) return GQA_ERR_INVALID_ARG;
+        ns = decode::auto_splits(gqa_attn_pick_num_splits, B, H_q, H_kv, S_max);
+        if (ns < 1) return ns;
     }
     const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
@@ -1625,10 +1643,8 @@ extern "C" int gqa_attn_decode_ring(const uint16_t* q, const uint16_t* k, const 
     if (B == 0) return GQA_OK;
     int ns = num_splits;
     if (ns == 0) {
-        const int sms = num_sms();
-        if (sms <= 0) return GQA_ERR_CUDA;
-        ns = gqa_attn_pick_num_splits(B, H_kv, capacity, sms);
-        if (ns < 1) return GQA_ERR_INVALID_ARG;
+        ns = decode::auto_splits(gqa_attn_pick_num_splits, B, H_q, H_kv, capacity);
+        if (ns < 1) return ns;
     }
     const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
@@ -1751,10 +1767,8 @@ extern "C" int gqa_attn_decode_q8(const uint16_t* q, const uint8_t* k_codes,
     if (B == 0) return GQA_OK;
     int ns = num_splits;
     if (ns == 0) {
-        const int sms = num_sms();
-        if (sms <= 0) return GQA_ERR_CUDA;
-        ns = gqa_attn_pick_num_splits_q8(B, H_kv, S_max, sms);
-        if (ns < 1) return GQA_ERR_INVALID_ARG;
+        ns = decode::auto_splits(gqa_attn_pick_num_splits_q8, B, H_q, H_kv, S_max);
+        if (ns < 1) return ns;
     }
     const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
@@ -1872,10 +1886,8 @@ extern "C" int gqa_attn_decode_q4(const uint16_t* q, const uint8_t* k_codes,
     if (B == 0) return GQA_OK;
     int ns = num_splits;
     if (ns == 0) {
-        const int sms = num_sms();
-        if (sms <= 0) return GQA_ERR_CUDA;
-        ns = gqa_attn_pick_num_splits_q4(B, H_kv, S_max, sms);
-        if (ns < 1) return GQA_ERR_INVALID_ARG;
+        ns = decode::auto_splits(gqa_attn_pick_num_splits_q4, B, H_q, H_kv, S_max);
+        if (ns < 1) return ns;
     }
     const size_t bytes = decode::launch_ws_bytes(B, H_q, H_kv, d, ns);
     void* ws = nullptr;
@@ -1955,10 +1967,8 @@ extern "C" int gqa_attn_decode_noalloc(const uint16_t* q, const uint16_t* k, con
     if (B == 0) return GQA_OK;
     int ns = num_splits;
     if (ns == 0) {
-        const int sms = num_sms();
-        if (sms <= 0) return GQA_ERR_CUDA;
-        ns = gqa_attn_pick_num_splits(B, H_kv, S_max, sms);
-        if (ns < 1) return GQA_ERR_INVALID_ARG;
+        ns = decode::auto_splits(gqa_attn_pick_num_splits, B, H_q, H_kv, S_max);
+        if (ns < 1) return ns;
     }
     const WsLayout wl = ws_layout(B, H_q, d, ns, cluster_size_for(ns, grid_ctas(ns, B, H_q, H_kv)));
     if (wl.total > kNoAllocScratchBytes) return GQA_ERR_WORKSPACE;

@@ -84,7 +84,11 @@ enum {
  * rank placement has no counterpart on one GPU): num_splits contiguous
  * chunks of L = ceil(S_max / num_splits) keys; split s of row b covers
  * [min(s*L, seqlen_b), min((s+1)*L, seqlen_b)). num_splits <= 0 picks it
- * with gqa_attn_pick_num_splits() for the current device.
+ * with gqa_attn_pick_num_splits(B, H_kv, S_max, SMs of the current device);
+ * for G > 8 (two CTAs per split and KV head, heads 0-7 and 8-15) the plan for
+ * 2 * H_kv heads is taken instead when B * 2 * H_kv * n <= SMs and its splits
+ * hold at most 1024 keys. gqa_attn_decode_partial, _ring and _noalloc resolve
+ * num_splits == 0 the same way; _q8 and _q4 use their own plan for H_kv.
  *
  *   q, k, v, o : see layouts above; 16-byte aligned.
  *   lse        : [B, H_q] fp32, or NULL to skip it. A row with seqlen 0 gets

@@ -128,6 +128,23 @@ def test_llama70b_decode_8k_all_rows():
         assert_close(o2, lse2, O.reshape(1, w.H_q, w.d), L.reshape(1, w.H_q), f"8k ns={ns}")
 
 
+@pytest.mark.parametrize("B,H_q,S,lens", [
+    (1, 128, 8192, None),                 # 128 query heads on 8 KV heads (G = 16): 8 splits
+    (2, 64, 8192, [8192, 5000]),          # two rows: one wave of 8-split clusters
+    (4, 64, 4096, [4096, 1, 0, 3333]),    # four rows: 4 splits of 1024 keys
+])
+def test_automatic_plans_every_row(B, H_q, S, lens):
+    # num_splits = 0 on shapes where the plan takes one wave of whole-row
+    # clusters (a G = 16 group counts as two CTAs per split and KV head);
+    # every row against the fp64 oracle.
+    H_kv, d = 8, 128
+    q, k, v, sl = wl.small_decode(B, H_q, H_kv, d, S, seed=560 + B + H_q, seqlens=lens)
+    o, lse = run_decode(q, k, v, sl, 0)
+    O, L = attention_by_group(q[:, :, None], k, v, scale=1 / math.sqrt(d),
+                              seqlens=None if sl is None else sl.tolist())
+    assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"B={B} H_q={H_q} S={S}")
+
+
 def test_ragged_long_context_every_row():
     # All 4 x 64 query-head rows of the ragged 128K batch (every (row, KV head)
     # group, padded cache masked by seqlens), against the fp64 oracle.
