@@ -26,28 +26,43 @@ namespace {
 
 constexpr int kMinKeysPerSplit = 256;   // below this a split is mostly ramp-up
 constexpr int kMaxKeysPerSplit = 1024;  // long rows spread over many blocks
-constexpr int kMaxKeysPerWaveSplit = 2048;  // split bound of the one-wave plan below
+// split bounds of the one-wave plan below: a batch of rows may be ragged (a long
+// row's splits would then set the time), a single row cannot
+constexpr int kMaxKeysPerWaveSplit = 2048;
+constexpr int kMaxKeysPerWaveSplitOneRow = 16384;
 constexpr int kMaxSplits = 8192;
 constexpr int kClusterSplits = 16;      // splits merged on chip by one thread-block cluster
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The split rule; one_row: the one-wave split bound for B == 1.
+int pick_splits(int B, int H_kv, int S_max, int num_sms, int64_t one_row);
+
 }  // namespace
 
+// The bf16 decode streams a single row best in one wave even with long
+// splits; the INT8 / INT4 decodes are bound by issue per SM and keep the
+// batch bound (their rule below).
 extern "C" int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms) {
+    return pick_splits(B, H_kv, S_max, num_sms, kMaxKeysPerWaveSplitOneRow);
+}
+
+namespace {
+
+int pick_splits(int B, int H_kv, int S_max, int num_sms, int64_t one_row) {
     if (B <= 0 || H_kv <= 0 || S_max <= 0 || num_sms <= 0) return GQA_ERR_INVALID_ARG;
     const int64_t pairs = int64_t(B) * H_kv;
     // One wave of whole-row clusters: the largest ns of 16, 8, 4, 2 whose
     // grid fits on the SMs, if it keeps >= 80% of them busy and its splits
-    // hold 256..2048 keys. Each row then merges on chip in one cluster and no
-    // combine kernel runs (GB300, 64/8 heads: B = 2 at 8K 13.9 us with 8
-    // splits against 19.6 with 10; B = 1 at 32K 24.3 us with 16 against 28.0
-    // with 32).
+    // hold 256..2048 keys (`one_row` for a single row). Each row then merges
+    // on chip in one cluster and no combine kernel runs (GB300, 64/8 heads:
+    // B = 2 at 8K 13.9 us with 8 splits against 19.6 with 10; B = 1 at 32K
+    // 24.3 us with 16 against 28.0 with 32, at 128K 82.4 against 89.2 with 128).
+    const int64_t wave_max = B == 1 ? one_row : kMaxKeysPerWaveSplit;
     for (int ns : {16, 8, 4, 2}) {
         if (pairs * ns > num_sms) continue;
         const int64_t keys = ceil_div(S_max, ns);
-        if (5 * pairs * ns >= 4 * int64_t(num_sms) && keys >= kMinKeysPerSplit &&
-            keys <= kMaxKeysPerWaveSplit)
+        if (5 * pairs * ns >= 4 * int64_t(num_sms) && keys >= kMinKeysPerSplit && keys <= wave_max)
             return ns;
         break;
     }
@@ -68,11 +83,15 @@ extern "C" int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms)
     return int(ns);
 }
 
+}  // namespace
+
 // An INT8 token carries about half the bytes of a bf16 one, and the bounds
-// above are per-split byte budgets written in bf16 keys.
+// above are per-split byte budgets written in bf16 keys; the one-wave bound
+// stays 2048 for a single row too (a CTA's issue rate, not HBM, bounds these
+// decodes).
 extern "C" int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_sms) {
     if (S_max <= 0) return GQA_ERR_INVALID_ARG;
-    return gqa_attn_pick_num_splits(B, H_kv, int((int64_t(S_max) + 1) / 2), num_sms);
+    return pick_splits(B, H_kv, int((int64_t(S_max) + 1) / 2), num_sms, kMaxKeysPerWaveSplit);
 }
 
 // INT4 takes the INT8 rule. Its token is about a quarter of a bf16 one in

@@ -337,8 +337,9 @@ GQA_API int gqa_attn_prefill_partial(const uint16_t* q, const uint16_t* k, const
 
 /* Split count for a decode problem. First, one wave of whole-row clusters:
  * the largest n of 16, 8, 4, 2 with B * H_kv * n <= num_sms, taken if
- * B * H_kv * n >= 0.8 * num_sms and 256 <= ceil(S_max / n) <= 2048 (every
- * row then merges on chip, with no combine kernel). Otherwise
+ * B * H_kv * n >= 0.8 * num_sms and 256 <= ceil(S_max / n) <= 2048, or
+ * <= 16384 when B == 1 (every row then merges on chip, with no combine
+ * kernel; the tighter bound guards ragged batches). Otherwise
  * n = ceil(num_sms / (B * H_kv)) blocks per row (when above 16, rounded down
  * to a multiple of 16 if the blocks then still cover >= 80% of the SMs), at
  * least ceil(S_max / 1024) (rounded up to a multiple of 16 when above 16), and
@@ -347,9 +348,11 @@ GQA_API int gqa_attn_prefill_partial(const uint16_t* q, const uint16_t* k, const
 GQA_API int gqa_attn_pick_num_splits(int B, int H_kv, int S_max, int num_sms);
 
 /* Split count for a decode over an INT8 cache: gqa_attn_pick_num_splits for a
- * row of ceil(S_max / 2) keys. The split-length bounds above are sized in
- * bytes, and an INT8 token (2 x d code bytes + 2 fp32 scales) is about half
- * a bf16 token (4 x d bytes). Returns >= 1, or GQA_ERR_INVALID_ARG. */
+ * row of ceil(S_max / 2) keys, except that the one-wave plan's bound stays
+ * 2048 keys for B == 1 too (these decodes are bound by each CTA's issue rate,
+ * not by HBM). The split-length bounds are sized in bytes, and an INT8 token
+ * (2 x d code bytes + 2 fp32 scales) is about half a bf16 token (4 x d
+ * bytes). Returns >= 1, or GQA_ERR_INVALID_ARG. */
 GQA_API int gqa_attn_pick_num_splits_q8(int B, int H_kv, int S_max, int num_sms);
 
 /* Split count for a decode over an INT4 cache: the INT8 rule,

@@ -85,13 +85,14 @@ def test_prefill_tile_counts_bit_exact_vs_oracle(L, T_q, S_kv, off, causal):
         assert fut == int((cls == orc.TILE_ALL_FUTURE).sum())
 
 
-def _pick_reference(B, H_kv, S, sms):
-    # The rule stated in include/gqa_attn.h, restated independently.
+def _pick_reference(B, H_kv, S, sms, one_row=16384):
+    # The rule stated in include/gqa_attn.h, restated independently
+    # (one_row: the one-wave split bound for B = 1; 2048 for the INT8 rule).
     cdiv = lambda a, b: -(-a // b)
     fits = [n for n in (16, 8, 4, 2) if B * H_kv * n <= sms]
     if fits:   # one wave of whole-row clusters, if it is busy enough
         n = fits[0]
-        if B * H_kv * n >= 0.8 * sms and 256 <= cdiv(S, n) <= 2048:
+        if B * H_kv * n >= 0.8 * sms and 256 <= cdiv(S, n) <= (one_row if B == 1 else 2048):
             return n
     n = cdiv(sms, B * H_kv)
     if n > 16 and B * H_kv * 16 * (n // 16) >= 0.8 * sms:
@@ -108,10 +109,12 @@ def test_pick_num_splits_bit_exact_and_properties(L):
     assert api.gqa_attn_pick_num_splits(1, 1, 256, 152) == 1         # tiny decode
     assert api.gqa_attn_pick_num_splits(2, 8, 8192, 152) == 8        # one wave, 8 clusters of 8
     assert api.gqa_attn_pick_num_splits(1, 8, 32768, 152) == 16      # one wave, 2048-key splits
-    assert api.gqa_attn_pick_num_splits(1, 8, 65536, 152) == 64      # 4096-key splits: no
+    assert api.gqa_attn_pick_num_splits(1, 8, 131072, 152) == 16     # one row: up to 16384 keys
+    assert api.gqa_attn_pick_num_splits(1, 8, 524288, 152) == 512    # 32768-key splits: no
+    assert api.gqa_attn_pick_num_splits(2, 8, 65536, 152) == 64      # a batch: 2048 at most
     for B, H_kv, S, sms in itertools.product((1, 2, 3, 4, 8, 64), (1, 2, 8),
                                              (1, 255, 256, 1000, 2048, 4096, 8192, 16384,
-                                              32768, 100000, 131072),
+                                              32768, 65536, 100000, 131072, 262144, 300000),
                                              (1, 148, 152)):
         ns = api.gqa_attn_pick_num_splits(B, H_kv, S, sms)
         assert ns == _pick_reference(B, H_kv, S, sms), (B, H_kv, S, sms)
@@ -126,10 +129,11 @@ def test_pick_num_splits_q8_plans_half_the_keys(L):
     # an INT8 token is about half the bytes of a bf16 one
     assert api.gqa_attn_pick_num_splits_q8(1, 8, 8192, 152) == 16     # 8K decode: unchanged
     assert api.gqa_attn_pick_num_splits_q8(4, 8, 131072, 152) == 64   # 128K ragged: half
-    for B, H_kv, S, sms in itertools.product((1, 4, 64), (1, 8), (1, 2, 255, 513, 8192, 131072),
-                                             (1, 152)):
+    assert api.gqa_attn_pick_num_splits_q8(1, 8, 131072, 152) == 64   # one row: bound 2048
+    for B, H_kv, S, sms in itertools.product((1, 4, 64), (1, 8),
+                                             (1, 2, 255, 513, 8192, 65536, 131072), (1, 152)):
         assert api.gqa_attn_pick_num_splits_q8(B, H_kv, S, sms) == \
-            _pick_reference(B, H_kv, -(-S // 2), sms), (B, H_kv, S, sms)
+            _pick_reference(B, H_kv, -(-S // 2), sms, one_row=2048), (B, H_kv, S, sms)
     assert api.gqa_attn_pick_num_splits_q8(1, 8, 0, 152) == api.GQA_ERR_INVALID_ARG
 
 
@@ -273,10 +277,10 @@ def test_pick_num_splits_q4_takes_the_int8_rule(L):
     # both quantised decodes are issue-bound: INT4 plans like INT8 (half the row)
     assert api.gqa_attn_pick_num_splits_q4(1, 8, 8192, 152) == 16     # 8K decode
     assert api.gqa_attn_pick_num_splits_q4(4, 8, 131072, 152) == 64   # 128K ragged
-    for B, H_kv, S, sms in itertools.product((1, 4, 64), (1, 8), (1, 2, 255, 513, 8192, 131072),
-                                             (1, 152)):
+    for B, H_kv, S, sms in itertools.product((1, 4, 64), (1, 8),
+                                             (1, 2, 255, 513, 8192, 65536, 131072), (1, 152)):
         assert api.gqa_attn_pick_num_splits_q4(B, H_kv, S, sms) == \
-            _pick_reference(B, H_kv, -(-S // 2), sms), (B, H_kv, S, sms)
+            _pick_reference(B, H_kv, -(-S // 2), sms, one_row=2048), (B, H_kv, S, sms)
     assert api.gqa_attn_pick_num_splits_q4(1, 8, 0, 152) == api.GQA_ERR_INVALID_ARG
 
 
