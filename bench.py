@@ -652,8 +652,9 @@ def run_case(args):
         work, unit = q8_bytes / 1e9, "GB/s"
         extra = {("int4" if int4 else "int8") + "_bytes_per_call": q8_bytes,
                  "bf16_equivalent_bytes_per_call": bf16_bytes}
-    elif args.case in ("decode8k", "ragged128k", "ring8k"):
-        w = wl.RAGGED_DECODE_128K if args.case == "ragged128k" else wl.LLAMA70B_DECODE_8K
+    elif args.case in ("decode8k", "ragged128k", "ring8k", "decode128k"):
+        w = {"ragged128k": wl.RAGGED_DECODE_128K,
+             "decode128k": wl.LLAMA70B_DECODE_128K_B1}.get(args.case, wl.LLAMA70B_DECODE_8K)
         q, k, v, sl = (t.to(dev) for t in wl.decode_inputs(w))
         ring = args.case == "ring8k"
         if ring:
@@ -752,9 +753,9 @@ def main():
                     help="CPU work per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="one workload alone: decode8k | ragged128k | ring8k | decode8k_q8 | "
-                         "ragged128k_q8 | decode8k_q4 | ragged128k_q4 | prefill8k | chunked32k "
-                         "| prefill8k_mha")
+                    help="one workload alone: decode8k | ragged128k | ring8k | decode128k | "
+                         "decode8k_q8 | ragged128k_q8 | decode8k_q4 | ragged128k_q4 | prefill8k "
+                         "| chunked32k | prefill8k_mha")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-worker-steps", type=int, default=1, help=argparse.SUPPRESS)

@@ -68,6 +68,11 @@ CHUNKED_PREFILL_32K = PrefillWorkload("llama70b_chunked_prefill_b2_t2048_off3072
 CAUSAL_PREFILL_8K_MHA = PrefillWorkload("mha_causal_prefill_b1_t8192", 1, 64, 64, 128, 8192,
                                         8192, 0, seed=6)
 
+# Not one of the five workloads: one sequence of 128K cached tokens (the
+# single-row long-context decode the split plan gives one wave of 16 splits).
+LLAMA70B_DECODE_128K_B1 = DecodeWorkload("llama70b_decode_b1_s131072", 1, 64, 8, 128, 131072,
+                                         seed=7)
+
 RAGGED_SEQLEN_SEED = 1003
 RAGGED_SEQLEN_RANGE = (16384, 131072)  # inclusive
 

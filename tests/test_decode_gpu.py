@@ -145,6 +145,16 @@ def test_automatic_plans_every_row(B, H_q, S, lens):
     assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"B={B} H_q={H_q} S={S}")
 
 
+def test_single_row_128k_every_head():
+    # One 128K row: the plan takes one wave of 16 splits of 8192 keys; all
+    # 64 query heads against the fp64 oracle.
+    w = wl.LLAMA70B_DECODE_128K_B1
+    q, k, v, sl = wl.decode_inputs(w)
+    o, lse = run_decode(q, k, v, sl, 0)
+    O, L = attention_by_group(q[:, :, None], k, v, scale=w.scale, seqlens=sl.tolist())
+    assert_close(o, lse, O[:, :, 0], L[:, :, 0], "128K single row")
+
+
 def test_ragged_long_context_every_row():
     # All 4 x 64 query-head rows of the ragged 128K batch (every (row, KV head)
     # group, padded cache masked by seqlens), against the fp64 oracle.
