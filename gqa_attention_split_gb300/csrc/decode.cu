@@ -1269,6 +1269,9 @@ int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStre
         rc = sp.warm_l2 ? launch_cs<D, kInt4, kQ4WarpsOneWave, kQ4StagesOneWave>(sp, cs, maps,
                                                                                  stream)
                         : launch_cs<D, kInt4, kQ4Warps, kQ4Stages>(sp, cs, maps, stream);
+    else if constexpr (D == 64)  // half-size stages: twice the stages keep as many bytes in flight
+        rc = sp.warm_l2 ? launch_cs<D, kBf16, 4, kStages>(sp, cs, maps, stream)
+                        : launch_cs<D, kBf16, 4, 2>(sp, cs, maps, stream);
     else
         rc = sp.warm_l2 ? launch_cs<D, kBf16, kWarps, kStages>(sp, cs, maps, stream)
                         : launch_cs<D, kBf16, 4, 1>(sp, cs, maps, stream);

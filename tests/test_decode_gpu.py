@@ -145,6 +145,19 @@ def test_automatic_plans_every_row(B, H_q, S, lens):
     assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"B={B} H_q={H_q} S={S}")
 
 
+@pytest.mark.parametrize("B,S,lens", [
+    (4, 8192, [8192, 8000, 4097, 31]),      # one wave of 4-split clusters, 6-stage rings
+    (5, 20000, [20000, 1, 19999, 777, 0]),  # more CTAs than SMs: 4 warps x 2 stages
+])
+def test_head_dim_64_every_row(B, S, lens):
+    # d = 64 streams 8 KB stages, twice as many per ring as d = 128
+    H_q, H_kv, d = 32, 8, 64
+    q, k, v, sl = wl.small_decode(B, H_q, H_kv, d, S, seed=580 + B, seqlens=lens)
+    o, lse = run_decode(q, k, v, sl, 0)
+    O, L = attention_by_group(q[:, :, None], k, v, scale=1 / math.sqrt(d), seqlens=sl.tolist())
+    assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"d=64 B={B} S={S}")
+
+
 def test_single_row_128k_every_head():
     # One 128K row: the plan takes one wave of 16 splits of 8192 keys; all
     # 64 query heads against the fp64 oracle.
