@@ -1263,7 +1263,10 @@ template <int D, int KIND>
 int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     int rc;
     if constexpr (KIND == kInt8)
-        rc = sp.warm_l2 ? launch_cs<D, kInt8, 4, 1>(sp, cs, maps, stream)
+        // one wave: 4 x 1 in clusters of 16 (the 8K single row), 3 x 2 in smaller
+        // clusters (the small-batch plans, whose CTAs walk more tiles)
+        rc = sp.warm_l2 ? (cs <= 8 ? launch_cs<D, kInt8, 3, 2>(sp, cs, maps, stream)
+                                   : launch_cs<D, kInt8, 4, 1>(sp, cs, maps, stream))
                         : launch_cs<D, kInt8, 3, 2>(sp, cs, maps, stream);
     else if constexpr (KIND == kInt4)
         rc = sp.warm_l2 ? launch_cs<D, kInt4, kQ4WarpsOneWave, kQ4StagesOneWave>(sp, cs, maps,

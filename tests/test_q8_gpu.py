@@ -122,6 +122,20 @@ def test_full_size_8k_decode_through_the_gpu_quantiser():
     assert np.abs(O - O16[:, :, 0]).max() < 0.05
 
 
+def test_small_batch_one_wave_every_row():
+    # B = 4 at 8K: the plan takes one wave of 4-split clusters (3 warps x 2
+    # stages per CTA); every row against attention over the oracle's cache
+    B, H_kv, G, S, d = 4, 8, 8, 8192, 128
+    lens = [8192, 6000, 64, 8191]
+    q, k, v, _ = wl.small_decode(B, G * H_kv, H_kv, d, S, seed=960, seqlens=lens)
+    kc, ks, vc, vs, dkc, dvc, dks, dvs = _oracle_cache(k, v)
+    o, lse = api.decode_q8(q.cuda(), dkc, dvc, dks, dvs,
+                           torch.tensor(lens, dtype=torch.int32).cuda())
+    api.check()
+    O, L = orc.attention_q8(q, kc, ks, vc, vs, scale=1 / math.sqrt(d), seqlens=lens)
+    _assert_close(o, lse, O, L, "B=4 8K one wave")
+
+
 def test_ragged_128k_every_head():
     # All 4 x 64 query-head rows of the ragged 128K batch over the GPU
     # quantiser's cache, against attention over the oracle's dequantised
