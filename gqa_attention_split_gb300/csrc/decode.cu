@@ -1117,9 +1117,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #define GQA_DEC_WARPS 2
 #endif
 constexpr int kTileT = GQA_DEC_TILE_T, kStages = GQA_DEC_STAGES, kWarps = GQA_DEC_WARPS;
-// int8 caches: 64 tokens per stage; a grid of one wave runs 2 warps x 3
-// stages per CTA, a longer grid 3 warps x 2 stages (GB300, 8K decode: 9.4 vs
-// 9.8 us; ragged 128K batch: 106 vs 97 us).
+// int8 caches: 64 tokens per stage; the warps x stages per CTA are chosen in
+// launch() below.
 constexpr int kTileTQ8 = 64;
 // int4 caches: 64 tokens per stage (8 KB of codes + 512 B of scales), 4 warps x
 // 2 stages per CTA on one-wave and longer grids alike (GB300: 8K decode 9.35 us,
@@ -1263,8 +1262,10 @@ template <int D, int KIND>
 int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStream_t stream) {
     int rc;
     if constexpr (KIND == kInt8)
-        // one wave: 4 x 1 in clusters of 16 (the 8K single row), 3 x 2 in smaller
-        // clusters (the small-batch plans, whose CTAs walk more tiles)
+        // one wave: 4 x 1 in clusters of 16 (the 8K single row: 8.67 us against
+        // 9.34 with 2 x 3), 3 x 2 in smaller clusters (the small-batch plans,
+        // whose CTAs walk more tiles) and in longer grids (ragged 128K batch:
+        // 86-88 us)
         rc = sp.warm_l2 ? (cs <= 8 ? launch_cs<D, kInt8, 3, 2>(sp, cs, maps, stream)
                                    : launch_cs<D, kInt8, 4, 1>(sp, cs, maps, stream))
                         : launch_cs<D, kInt8, 3, 2>(sp, cs, maps, stream);
@@ -1272,7 +1273,10 @@ int launch(const SplitParams& sp, int cs, const CUtensorMap (&maps)[4], cudaStre
         rc = sp.warm_l2 ? launch_cs<D, kInt4, kQ4WarpsOneWave, kQ4StagesOneWave>(sp, cs, maps,
                                                                                  stream)
                         : launch_cs<D, kInt4, kQ4Warps, kQ4Stages>(sp, cs, maps, stream);
-    else if constexpr (D == 64)  // half-size stages: twice the stages keep as many bytes in flight
+    else if constexpr (D == 64)
+        // half-size stages: twice the warps (one wave) or the stages (longer
+        // grids) keep d = 128's bytes in flight, and 4 warps per CTA hide the
+        // per-tile softmax work that half the bytes per key leaves exposed
         rc = sp.warm_l2 ? launch_cs<D, kBf16, 4, kStages>(sp, cs, maps, stream)
                         : launch_cs<D, kBf16, 4, 2>(sp, cs, maps, stream);
     else
