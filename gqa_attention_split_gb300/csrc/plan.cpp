@@ -30,6 +30,9 @@ constexpr int kMaxKeysPerSplit = 1024;  // long rows spread over many blocks
 // row's splits would then set the time), a single row cannot
 constexpr int kMaxKeysPerWaveSplit = 2048;
 constexpr int kMaxKeysPerWaveSplitOneRow = 16384;
+// splits this short take the one-wave plan even with fewer than 80% of the SMs
+// busy: a combine launch costs more than the idle SMs
+constexpr int kShortSplitKeys = 512;
 constexpr int kMaxSplits = 8192;
 constexpr int kClusterSplits = 16;      // splits merged on chip by one thread-block cluster
 
@@ -54,16 +57,18 @@ int pick_splits(int B, int H_kv, int S_max, int num_sms, int64_t one_row) {
     const int64_t pairs = int64_t(B) * H_kv;
     // One wave of whole-row clusters: the largest ns of 16, 8, 4, 2 whose
     // grid fits on the SMs, if it keeps >= 80% of them busy and its splits
-    // hold 256..2048 keys (`one_row` for a single row). Each row then merges
-    // on chip in one cluster and no combine kernel runs (GB300, 64/8 heads:
-    // B = 2 at 8K 13.9 us with 8 splits against 19.6 with 10; B = 1 at 32K
-    // 24.3 us with 16 against 28.0 with 32, at 128K 82.4 against 89.2 with 128).
+    // hold 256..2048 keys (`one_row` for a single row), or if its splits hold
+    // 256..512 keys however many SMs it uses. Each row then merges on chip in
+    // one cluster and no combine kernel runs (GB300, 64/8 heads: B = 2 at 8K
+    // 13.9 us with 8 splits against 19.6 with 10; B = 1 at 32K 24.3 us with
+    // 16 against 28.0 with 32, at 128K 82.4 against 89.2 with 128; 28/4 heads,
+    // B = 1 at 8K: 7.6 us with 16 splits on 64 CTAs against 8.9 with 32).
     const int64_t wave_max = B == 1 ? one_row : kMaxKeysPerWaveSplit;
     for (int ns : {16, 8, 4, 2}) {
         if (pairs * ns > num_sms) continue;
         const int64_t keys = ceil_div(S_max, ns);
-        if (5 * pairs * ns >= 4 * int64_t(num_sms) && keys >= kMinKeysPerSplit && keys <= wave_max)
-            return ns;
+        const bool busy = 5 * pairs * ns >= 4 * int64_t(num_sms) && keys <= wave_max;
+        if (keys >= kMinKeysPerSplit && (busy || keys <= kShortSplitKeys)) return ns;
         break;
     }
     // Otherwise enough blocks to cover the SMs at low batch, in whole clusters of

@@ -338,8 +338,9 @@ GQA_API int gqa_attn_prefill_partial(const uint16_t* q, const uint16_t* k, const
 /* Split count for a decode problem. First, one wave of whole-row clusters:
  * the largest n of 16, 8, 4, 2 with B * H_kv * n <= num_sms, taken if
  * B * H_kv * n >= 0.8 * num_sms and 256 <= ceil(S_max / n) <= 2048, or
- * <= 16384 when B == 1 (every row then merges on chip, with no combine
- * kernel; the tighter bound guards ragged batches). Otherwise
+ * <= 16384 when B == 1 (the tighter bound guards ragged batches), or, with
+ * fewer SMs busy, if 256 <= ceil(S_max / n) <= 512 (every row then merges on
+ * chip, with no combine kernel). Otherwise
  * n = ceil(num_sms / (B * H_kv)) blocks per row (when above 16, rounded down
  * to a multiple of 16 if the blocks then still cover >= 80% of the SMs), at
  * least ceil(S_max / 1024) (rounded up to a multiple of 16 when above 16), and

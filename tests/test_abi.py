@@ -92,7 +92,9 @@ def _pick_reference(B, H_kv, S, sms, one_row=16384):
     fits = [n for n in (16, 8, 4, 2) if B * H_kv * n <= sms]
     if fits:   # one wave of whole-row clusters, if it is busy enough
         n = fits[0]
-        if B * H_kv * n >= 0.8 * sms and 256 <= cdiv(S, n) <= (one_row if B == 1 else 2048):
+        keys = cdiv(S, n)
+        busy = B * H_kv * n >= 0.8 * sms and keys <= (one_row if B == 1 else 2048)
+        if keys >= 256 and (busy or keys <= 512):
             return n
     n = cdiv(sms, B * H_kv)
     if n > 16 and B * H_kv * 16 * (n // 16) >= 0.8 * sms:
@@ -112,15 +114,19 @@ def test_pick_num_splits_bit_exact_and_properties(L):
     assert api.gqa_attn_pick_num_splits(1, 8, 131072, 152) == 16     # one row: up to 16384 keys
     assert api.gqa_attn_pick_num_splits(1, 8, 524288, 152) == 512    # 32768-key splits: no
     assert api.gqa_attn_pick_num_splits(2, 8, 65536, 152) == 64      # a batch: 2048 at most
-    for B, H_kv, S, sms in itertools.product((1, 2, 3, 4, 8, 64), (1, 2, 8),
+    assert api.gqa_attn_pick_num_splits(1, 4, 8192, 152) == 16       # short splits, 64 CTAs
+    assert api.gqa_attn_pick_num_splits(1, 4, 32768, 152) == 32      # 2048-key splits: no
+    for B, H_kv, S, sms in itertools.product((1, 2, 3, 4, 8, 64), (1, 2, 4, 6, 8),
                                              (1, 255, 256, 1000, 2048, 4096, 8192, 16384,
                                               32768, 65536, 100000, 131072, 262144, 300000),
                                              (1, 148, 152)):
         ns = api.gqa_attn_pick_num_splits(B, H_kv, S, sms)
         assert ns == _pick_reference(B, H_kv, S, sms), (B, H_kv, S, sms)
         assert 1 <= ns <= max(1, S // 256)
-        # the blocks cover at least 80% of the SMs whenever the length allows
-        if S // 256 >= -(-sms // (B * H_kv)):
+        # the blocks cover at least 80% of the SMs whenever the length allows,
+        # unless short splits (<= 512 keys) fit in one wave of whole-row clusters
+        short_wave = ns in (16, 8, 4, 2) and B * H_kv * ns <= sms and -(-S // ns) <= 512
+        if S // 256 >= -(-sms // (B * H_kv)) and not short_wave:
             assert B * H_kv * ns >= 0.8 * sms
     assert api.gqa_attn_pick_num_splits(0, 8, 8192, 152) == api.GQA_ERR_INVALID_ARG
 
