@@ -158,6 +158,34 @@ def test_head_dim_64_every_row(B, S, lens):
     assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"d=64 B={B} S={S}")
 
 
+def _random_decode_shapes(n, seed):
+    """Seeded shapes across the split plan's clauses (one wave at any SM use,
+    multi-wave with a combine, G > 8 as two CTAs per split), small enough for
+    the oracle: (B, H_q, H_kv, d, S_max, seqlens)."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    while len(shapes) < n:
+        B = int(rng.integers(1, 7))
+        H_kv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.integers(1, 17))
+        d = int(rng.choice([64, 128]))
+        S = int(rng.choice([1, 200, 1000, 3000, 8192, 20000]))
+        if B * H_kv * G * S * d > 60_000_000:
+            continue
+        lens = [int(x) for x in rng.integers(0, S + 1, size=B)]
+        lens[0] = S  # one full row
+        shapes.append((B, H_kv * G, H_kv, d, S, lens))
+    return shapes
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,d,S,lens", _random_decode_shapes(16, 2024))
+def test_random_shapes_automatic_plan(B, H_q, H_kv, d, S, lens):
+    q, k, v, sl = wl.small_decode(B, H_q, H_kv, d, S, seed=7000 + B * S + H_q, seqlens=lens)
+    o, lse = run_decode(q, k, v, sl, 0)
+    O, L = attention_by_group(q[:, :, None], k, v, scale=1 / math.sqrt(d), seqlens=lens)
+    assert_close(o, lse, O[:, :, 0], L[:, :, 0], f"B={B} H={H_q}/{H_kv} d={d} S={S} {lens}")
+
+
 def test_single_row_128k_every_head():
     # One 128K row: the plan takes one wave of 16 splits of 8192 keys; all
     # 64 query heads against the fp64 oracle.

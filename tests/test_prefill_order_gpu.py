@@ -68,6 +68,40 @@ def test_host_order_matches_closed_form_bitwise_and_the_oracle(B, H_q, H_kv, d, 
     assert np.abs(l1.cpu().double().numpy() - L).max() <= 1e-3
 
 
+def _random_prefill_shapes(n, seed):
+    """Seeded shapes for the prefill under both orders, small enough for the
+    oracle: (B, H_q, H_kv, d, T_q, S_kv, q_offset, causal)."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    while len(shapes) < n:
+        B = int(rng.integers(1, 4))
+        H_kv = int(rng.choice([1, 2, 4]))
+        G = int(rng.integers(1, 9))
+        d = int(rng.choice([64, 128]))
+        causal = bool(rng.integers(0, 2))
+        T = int(rng.integers(1, 1200))
+        off = int(rng.integers(0, 1500)) if causal else 0
+        S = T + off + (0 if causal else int(rng.integers(0, 800)))
+        if B * H_kv * G * T * S * d > 2_000_000_000:
+            continue
+        shapes.append((B, H_kv * G, H_kv, d, T, S, off, causal))
+    return shapes
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,d,T_q,S_kv,off,causal", _random_prefill_shapes(12, 77))
+def test_random_shapes_both_orders(B, H_q, H_kv, d, T_q, S_kv, off, causal):
+    q, k, v = wl.small_prefill(B, H_q, H_kv, d, T_q, S_kv, off, seed=900 + T_q + S_kv)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    (o0, l0), (o1, l1) = _both_orders(
+        lambda: api.prefill(qd, kd, vd, q_offset=off, causal=causal))
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    O, L = attention_by_group(q, k, v, scale=1 / math.sqrt(d), causal=causal, q_offset=off)
+    o = o1.float().cpu().double().numpy()
+    err = np.abs(o - O)
+    assert err.max() <= 1e-2 and err.mean() <= 1e-3
+    assert np.abs(l1.cpu().double().numpy() - L).max() <= 1e-3
+
+
 @pytest.mark.parametrize("G", [8, 3])
 def test_slice_prefill_under_a_host_order(G):
     # a key slice that starts past some query blocks: items with no visible key
